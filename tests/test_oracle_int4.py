@@ -1,0 +1,157 @@
+"""Pins for the oracle's INT4 asymmetric RTN quantizer, packing and dequantization.
+
+Each test checks a property the pages or the mathematics fix, chosen so that a
+plausible slip (a dropped zero point, a wrong sign, a swapped nibble order, a
+group index taken along the wrong axis) fails at least one of them.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import int4, numerics
+from synth import act_order_g_idx, gaussian_weights, student_t_weights
+
+
+def _quant(W, g_idx=None, gs=128):
+    q, s, z = int4.rtn_quantize(W, gs, g_idx)
+    return q, s, z
+
+
+@pytest.mark.parametrize("dist", ["normal", "t5"])
+def test_grid_invariant_and_levels(dist):
+    K, N = 512, 96
+    W = gaussian_weights(K, N, 0.02, 1) if dist == "normal" else student_t_weights(K, N, 5, 0.01, 1)
+    q, s, z = _quant(W)
+    assert q.max() <= 15 and z.max() <= 15  # 16 levels
+    w_hat = int4.dequant_exact(q, s, z)
+    s_rows = s.astype(np.float64)[np.arange(K) // 128]
+    z_rows = z.astype(np.float64)[np.arange(K) // 128]
+    ratio = w_hat / s_rows
+    # every reconstruction sits exactly on the integer grid (q - z) * s
+    assert np.array_equal(ratio, np.round(ratio))
+    assert np.all(ratio >= -z_rows) and np.all(ratio <= 15 - z_rows)
+
+
+def test_zero_is_exactly_representable():
+    # asymmetric quantization stores the zero point so that 0.0 maps to an
+    # integer code and reconstructs to exactly 0
+    W = gaussian_weights(256, 64, 0.02, 5)
+    W[::7, ::3] = 0.0
+    q, s, z = _quant(W)
+    w_hat = int4.dequant_exact(q, s, z)
+    assert np.all(w_hat[::7, ::3] == 0.0)
+
+
+def test_half_step_error_bound():
+    K, N = 1024, 128
+    W = student_t_weights(K, N, 5, 0.01, 2)
+    q, s, z = _quant(W)
+    w_hat = int4.dequant_exact(q, s, z)
+    s_rows = s.astype(np.float64)[np.arange(K) // 128]
+    err = np.abs(W.astype(np.float64) - w_hat)
+    clamped = (q == 0) | (q == 15)
+    # nearest-grid rounding: at most half a step away, wherever no clamp acted
+    interior = ~clamped
+    assert np.all(err[interior] <= s_rows[interior] / 2)
+    # at the ends the fp16 rounding of s can push min/max just outside the
+    # 15-step grid; the bound there is (1/2 + 15 * 2^-11 * (1 + 2^-11)) * s
+    bound = (0.5 + 15 * 2.0 ** -11 * (1 + 2.0 ** -11)) * s_rows
+    assert np.all(err <= bound)
+
+
+def test_lossless_on_exact_grid():
+    # weights built on a grid the quantizer can represent exactly must come back
+    # unchanged, with the grid's own scale, zero point and codes
+    rng = np.random.default_rng(11)
+    K, N = 256, 40
+    s0 = 2.0 ** -6
+    z0 = rng.integers(0, 16, size=(K // 128, N))
+    q0 = rng.integers(0, 16, size=(K, N))
+    q0[::128] = 0  # each group-column holds code 0 and code 15, so min/max
+    q0[1::128] = 15  # span exactly 15 steps
+    zr = z0[np.arange(K) // 128]
+    W = ((q0 - zr) * s0).astype(np.float32)
+    # groups with z0 == 0 or 15 have a zero end point already; others include 0
+    q, s, z = _quant(W)
+    assert np.all(s.astype(np.float64) == s0)
+    assert np.array_equal(z, z0.astype(np.uint8))
+    assert np.array_equal(q, q0.astype(np.uint8))
+    assert np.array_equal(int4.dequant_exact(q, s, z), W.astype(np.float64))
+
+
+def test_monotone_in_w_within_group():
+    K, N = 128, 64
+    W = gaussian_weights(K, N, 0.02, 9)
+    q, s, z = _quant(W)
+    order = np.argsort(W, axis=0, kind="stable")
+    qs = np.take_along_axis(q.astype(int), order, axis=0)
+    assert np.all(np.diff(qs, axis=0) >= 0)
+
+
+def test_pack_unpack_roundtrip_exhaustive_positions():
+    # every code value at every nibble position of a word
+    K, N = 8 * 16, 8
+    q = np.zeros((K, N), dtype=np.uint8)
+    for v in range(16):
+        for j in range(8):
+            q[8 * v + j, j] = v
+    p = int4.pack_along_k(q)
+    assert np.array_equal(int4.unpack_along_k(p), q)
+    rng = np.random.default_rng(0)
+    words = rng.integers(0, 2 ** 32, size=(64, 24), dtype=np.uint64).astype(np.uint32)
+    assert np.array_equal(int4.pack_along_k(int4.unpack_along_k(words)), words)
+    zw = rng.integers(0, 2 ** 32, size=(5, 3), dtype=np.uint64).astype(np.uint32)
+    assert np.array_equal(int4.pack_zeros(int4.unpack_zeros(zw)), zw)
+
+
+def test_pack_nibble_order():
+    # row 8i+j of a column lands in bits 4j..4j+3 of word [i, n]; zero point of
+    # column 8c+j lands in bits 4j.. of word [g, c]
+    q = np.arange(8, dtype=np.uint8).reshape(8, 1)
+    assert int4.pack_along_k(q)[0, 0] == 0x76543210
+    z = (np.arange(8, dtype=np.uint8) + 1).reshape(1, 8)
+    assert int4.pack_zeros(z)[0, 0] == 0x87654321
+
+
+def test_dequant_single_rounding():
+    # the dtype value is the exact (q - z) * s rounded once; forming
+    # q*s - z*s in the dtype instead differs on some inputs
+    rng = np.random.default_rng(4)
+    K, N = 128, 512
+    q = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    z = rng.integers(0, 16, size=(1, N)).astype(np.uint8)
+    s = numerics.to_f16(rng.uniform(1e-4, 0.1, size=(1, N)))
+    for dt in ("f16", "bf16"):
+        bits = int4.dequant(q, s, z, dt)
+        exact = int4.dequant_exact(q, s, z)
+        back = numerics.dtype_bits_to_f64(bits, dt)
+        # nearest representable: no other dtype value is closer
+        nxt = numerics.dtype_bits_to_f64(bits + np.uint16(1), dt)
+        prv = numerics.dtype_bits_to_f64(bits - np.uint16(1), dt)
+        err = np.abs(back - exact)
+        pos = back > 0
+        assert np.all(err[pos] <= np.abs(nxt[pos] - exact[pos]))
+        assert np.all(err[pos] <= np.abs(prv[pos] - exact[pos]))
+
+
+def test_act_order_equals_physical_regroup():
+    # quantizing with a scattered row->group map must give the same codes as
+    # first moving each group's rows together and quantizing contiguous groups
+    K, N = 1024, 48
+    W = student_t_weights(K, N, 5, 0.01, 3)
+    g_idx = act_order_g_idx(K, 128, 3)
+    q, s, z = _quant(W, g_idx)
+    order = np.argsort(g_idx, kind="stable")  # rows sorted by group
+    q2, s2, z2 = _quant(W[order])
+    assert np.array_equal(q[order], q2)
+    assert np.array_equal(s, s2) and np.array_equal(z, z2)
+    # and dequantization follows the map row by row
+    w1 = int4.dequant_exact(q, s, z, 128, g_idx)
+    w2 = int4.dequant_exact(q2, s2, z2)
+    assert np.array_equal(w1[order], w2)
+
+
+def test_g_idx_groups_have_group_size_rows():
+    g = act_order_g_idx(4096, 128, 0)
+    assert np.all(np.bincount(g) == 128)
+    assert not np.array_equal(g, np.arange(4096) // 128)
