@@ -1,0 +1,224 @@
+"""Python binding of the W4A16 / NF4 C-ABI library (``libw4a16.so``).
+
+Argument marshalling only: tensors are checked for dtype/shape/device, their
+device pointers and the current CUDA stream are handed to the C entry points,
+and every step of the computation runs in the library's CUDA kernels.  There
+is no CPU fallback: if the library is missing, importing this package raises.
+
+Tensor conventions (all CUDA, contiguous):
+  X        [M, K]  torch.float16 / torch.bfloat16
+  qweight  [K/8, N] torch.int32 (bit pattern of the packed uint32 words)
+  scales   [K/128, N] torch.float16
+  qzeros   [K/128, N/8] torch.int32
+  g_idx    [K] torch.int32 or None
+  absmax   [K/64, N] torch.float32 (NF4)
+  codebook [16] torch.float32 (NF4)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libw4a16.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"{_LIB_PATH} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+_SIGS = {
+    "w4a16_gemm": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
+    "w4a16_gemv": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
+    "nf4_gemm": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
+    "w4a16_dequant": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
+    "nf4_dequant": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
+    "w4a16_quantize": [_vp, _i, _i, _i, _vp, _vp, _vp, _vp],
+    "nf4_quantize": [_vp, _i, _i, _i, _vp, _vp, _vp, _vp],
+    "w4a16_workspace_bytes": [_i, _i, _i],
+    "w4a16_status_string": [_i],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _i
+_lib.w4a16_workspace_bytes.restype = _sz
+_lib.w4a16_status_string.restype = ctypes.c_char_p
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+GEMV_MAX_M = 16
+GROUP_SIZE = 128
+NF4_BLOCK = 64
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+
+EXPORTED = tuple(_SIGS)
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, fn: str):
+        self.status = status
+        super().__init__(f"{fn}: {_lib.w4a16_status_string(status).decode()} (status {status})")
+
+
+def _check(status: int, fn: str):
+    if status != OK:
+        raise W4A16Error(status, fn)
+
+
+def status_string(status: int) -> str:
+    return _lib.w4a16_status_string(status).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_lib.w4a16_workspace_bytes(M, N, K))
+
+
+_workspaces: dict = {}
+
+
+def workspace(M: int, N: int, K: int, device=None) -> torch.Tensor | None:
+    """A zero-initialised workspace big enough for (M, N, K), cached per device and stream.
+
+    Calls on one stream run in order, so sharing one buffer between them is
+    safe; each stream gets its own.
+    """
+    n = workspace_bytes(M, N, K)
+    if n == 0:
+        return None
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.zeros(max(n, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def _check_x(X, K):
+    if X.dtype not in _DTYPES or not X.is_cuda or X.dim() != 2 or X.shape[1] != K or not X.is_contiguous():
+        raise ValueError("X must be a contiguous CUDA [M, K] float16/bfloat16 tensor")
+
+
+def _out(X, N, out):
+    M = X.shape[0]
+    if out is None:
+        return torch.empty((M, N), dtype=X.dtype, device=X.device)
+    if out.shape != (M, N) or out.dtype != X.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] tensor of X's dtype")
+    return out
+
+
+def _int4_call(fn, X, qweight, scales, qzeros, g_idx, out, group_size, ws, dev_status):
+    K = qweight.shape[0] * 8
+    N = qweight.shape[1]
+    _check_x(X, K)
+    M = X.shape[0]
+    Y = _out(X, N, out)
+    if ws is None:
+        ws = workspace(M, N, K, X.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = getattr(_lib, fn)(_ptr(X), _ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx), _ptr(Y), M, N, K,
+                           group_size, _DTYPES[X.dtype], _ptr(ws), nbytes, _ptr(dev_status), _stream(X.device))
+    _check(st, fn)
+    return Y
+
+
+def gemm(X, qweight, scales, qzeros, g_idx=None, out=None, group_size=GROUP_SIZE, ws=None, dev_status=None):
+    """Y = X . W_hat (INT4), any M."""
+    return _int4_call("w4a16_gemm", X, qweight, scales, qzeros, g_idx, out, group_size, ws, dev_status)
+
+
+def gemv(X, qweight, scales, qzeros, g_idx=None, out=None, group_size=GROUP_SIZE, ws=None, dev_status=None):
+    """Y = X . W_hat (INT4), M <= 16 (the split-K decode kernel)."""
+    return _int4_call("w4a16_gemv", X, qweight, scales, qzeros, g_idx, out, group_size, ws, dev_status)
+
+
+def nf4_gemm(X, qweight, absmax, codebook, out=None, blocksize=NF4_BLOCK, ws=None, dev_status=None):
+    """Y = X . W_hat (NF4), any M."""
+    K = qweight.shape[0] * 8
+    N = qweight.shape[1]
+    _check_x(X, K)
+    M = X.shape[0]
+    Y = _out(X, N, out)
+    if ws is None:
+        ws = workspace(M, N, K, X.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _lib.nf4_gemm(_ptr(X), _ptr(qweight), _ptr(absmax), _ptr(codebook), _ptr(Y), M, N, K, blocksize,
+                       _DTYPES[X.dtype], _ptr(ws), nbytes, _ptr(dev_status), _stream(X.device))
+    _check(st, "nf4_gemm")
+    return Y
+
+
+def dequant(qweight, scales, qzeros, g_idx=None, dtype=torch.bfloat16, group_size=GROUP_SIZE):
+    """W_hat [K, N] in ``dtype`` (bit-exact dequantization)."""
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    W = torch.empty((K, N), dtype=dtype, device=qweight.device)
+    st = _lib.w4a16_dequant(_ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(g_idx), _ptr(W), K, N, group_size,
+                            _DTYPES[dtype], _stream(qweight.device))
+    _check(st, "w4a16_dequant")
+    return W
+
+
+def nf4_dequant(qweight, absmax, codebook, dtype=torch.bfloat16, blocksize=NF4_BLOCK):
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    W = torch.empty((K, N), dtype=dtype, device=qweight.device)
+    st = _lib.nf4_dequant(_ptr(qweight), _ptr(absmax), _ptr(codebook), _ptr(W), K, N, blocksize, _DTYPES[dtype],
+                          _stream(qweight.device))
+    _check(st, "nf4_dequant")
+    return W
+
+
+def quantize(W, group_size=GROUP_SIZE):
+    """RTN INT4 quantization of fp32 CUDA ``W[K, N]`` -> (qweight, scales, qzeros)."""
+    if W.dtype != torch.float32 or not W.is_cuda or not W.is_contiguous():
+        raise ValueError("W must be a contiguous CUDA float32 tensor")
+    K, N = W.shape
+    dev = W.device
+    qweight = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
+    scales = torch.empty((K // group_size, N), dtype=torch.float16, device=dev)
+    qzeros = torch.empty((K // group_size, N // 8), dtype=torch.int32, device=dev)
+    st = _lib.w4a16_quantize(_ptr(W), K, N, group_size, _ptr(qweight), _ptr(scales), _ptr(qzeros), _stream(dev))
+    _check(st, "w4a16_quantize")
+    return qweight, scales, qzeros
+
+
+def nf4_quantize(W, codebook, blocksize=NF4_BLOCK):
+    """NF4 quantization of fp32 CUDA ``W[K, N]`` -> (qweight, absmax)."""
+    if W.dtype != torch.float32 or not W.is_cuda or not W.is_contiguous():
+        raise ValueError("W must be a contiguous CUDA float32 tensor")
+    K, N = W.shape
+    dev = W.device
+    qweight = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
+    absmax = torch.empty((K // blocksize, N), dtype=torch.float32, device=dev)
+    st = _lib.nf4_quantize(_ptr(W), K, N, blocksize, _ptr(codebook), _ptr(qweight), _ptr(absmax), _stream(dev))
+    _check(st, "nf4_quantize")
+    return qweight, absmax
+
+
+def nf4_codebook(device="cuda") -> torch.Tensor:
+    """The 16-entry NF4 table: 0, 7 negative and 8 positive standard-normal
+    quantiles of evenly spaced probabilities up to 1 - (1/30 + 1/32)/2,
+    normalised to [-1, 1] (computed here in float64, stored as float32)."""
+    delta = 1.0 - 0.5 * (1.0 / 30.0 + 1.0 / 32.0)
+    d = torch.tensor(delta, dtype=torch.float64)
+    top = torch.special.ndtri(d)
+    pos = torch.special.ndtri(d - (d - 0.5) * torch.arange(8, dtype=torch.float64) / 8) / top
+    neg = -torch.special.ndtri(d - (d - 0.5) * torch.arange(7, dtype=torch.float64) / 7) / top
+    vals = torch.sort(torch.cat([neg, torch.zeros(1, dtype=torch.float64), pos])).values
+    return vals.to(torch.float32).to(device)

@@ -1,0 +1,207 @@
+// C ABI: argument validation and dispatch (see include/w4a16.h).
+//
+// Every entry point validates its arguments on the host and returns
+// W4A16_ERR_INVALID_ARG / W4A16_ERR_UNSUPPORTED without launching anything
+// when they are wrong; otherwise it enqueues its kernel(s) on the caller's
+// stream and returns the launch status.
+#include "w4a16.h"
+
+#include <cstdint>
+
+#include "w4a16_internal.h"
+
+using namespace w4a16;
+
+namespace {
+
+constexpr int kInt4Group = 128;
+constexpr int kNF4Block = 64;
+constexpr int kMaxK = 65535 * 8;  // word-rows index a grid dimension
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+bool ok_dtype(w4a16_dtype d) { return d == W4A16_F16 || d == W4A16_BF16; }
+
+w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+// Shape checks common to the INT4 entry points.  Returns OK, or the error.
+w4a16_status check_int4_shape(int M, int N, int K, int group_size) {
+  if (M < 0 || N < 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+  if (N % 8 || K % 8 || K > kMaxK) return W4A16_ERR_INVALID_ARG;
+  if (group_size <= 0 || K % group_size) return W4A16_ERR_INVALID_ARG;
+  if (group_size != kInt4Group) return W4A16_ERR_UNSUPPORTED;
+  return W4A16_OK;
+}
+
+w4a16_status check_nf4_shape(int M, int N, int K, int blocksize) {
+  if (M < 0 || N < 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+  if (N % 8 || K % 8 || K > kMaxK) return W4A16_ERR_INVALID_ARG;
+  if (blocksize <= 0 || K % blocksize) return W4A16_ERR_INVALID_ARG;
+  if (blocksize != kNF4Block) return W4A16_ERR_UNSUPPORTED;
+  return W4A16_OK;
+}
+
+w4a16_status check_workspace(const GemvPlan& p, void* ws, size_t ws_bytes) {
+  if (p.workspace_bytes == 0) return W4A16_OK;
+  if (!ok_ptr(ws) || ws_bytes < p.workspace_bytes) return W4A16_ERR_INVALID_ARG;
+  return W4A16_OK;
+}
+
+GemvArgs gemv_args(const void* X, const uint32_t* qw, void* Y, int M, int N, int K, const GemvPlan& p,
+                   void* ws) {
+  GemvArgs a{};
+  a.X = static_cast<const uint16_t*>(X);
+  a.qw = qw;
+  a.Y = static_cast<uint16_t*>(Y);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.G = (K + 127) / 128;
+  a.groups_per_split = p.groups_per_split;
+  a.splits = p.splits;
+  if (p.splits > 1) {
+    a.counters = static_cast<int*>(ws);
+    a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + p.counters_bytes);
+  }
+  return a;
+}
+
+w4a16_status int4_gemv_impl(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                            const int32_t* g_idx, void* Y, int M, int N, int K, w4a16_dtype dtype,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const GemvPlan p = gemv_plan(M, N, K, kInt4Group);
+  w4a16_status st = check_workspace(p, workspace, workspace_bytes);
+  if (st != W4A16_OK) return st;
+  GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace);
+  a.scales = static_cast<const uint16_t*>(scales);
+  a.qz = qzeros;
+  a.g_idx = g_idx;
+  return from_cuda(launch_gemv_int4(a, dtype == W4A16_BF16, stream));
+}
+
+w4a16_status check_int4_ptrs(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                             const int32_t* g_idx, const void* Y) {
+  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(qzeros) || !ok_ptr(Y))
+    return W4A16_ERR_INVALID_ARG;
+  if (g_idx && !aligned16(g_idx)) return W4A16_ERR_INVALID_ARG;
+  return W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                        const int32_t* g_idx, void* Y, int M, int N, int K, int group_size, w4a16_dtype dtype,
+                        void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  (void)dev_status;
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_int4_shape(M, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (M > W4A16_GEMV_MAX_M) return W4A16_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return W4A16_OK;
+  st = check_int4_ptrs(X, qweight, scales, qzeros, g_idx, Y);
+  if (st != W4A16_OK) return st;
+  return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes, stream);
+}
+
+w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                        const int32_t* g_idx, void* Y, int M, int N, int K, int group_size, w4a16_dtype dtype,
+                        void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_int4_shape(M, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (M == 0 || N == 0) return W4A16_OK;
+  st = check_int4_ptrs(X, qweight, scales, qzeros, g_idx, Y);
+  if (st != W4A16_OK) return st;
+  if (M <= W4A16_GEMV_MAX_M)
+    return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
+                          stream);
+  (void)dev_status;
+  return W4A16_ERR_UNSUPPORTED;
+}
+
+w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absmax, const float* codebook16,
+                      void* Y, int M, int N, int K, int blocksize, w4a16_dtype dtype, void* workspace,
+                      size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_nf4_shape(M, N, K, blocksize);
+  if (st != W4A16_OK) return st;
+  if (M == 0 || N == 0) return W4A16_OK;
+  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(codebook16) || !ok_ptr(Y))
+    return W4A16_ERR_INVALID_ARG;
+  if (M <= W4A16_GEMV_MAX_M) {
+    const GemvPlan p = gemv_plan(M, N, K, kNF4Block);
+    st = check_workspace(p, workspace, workspace_bytes);
+    if (st != W4A16_OK) return st;
+    GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace);
+    a.absmax = absmax;
+    a.codebook = codebook16;
+    return from_cuda(launch_gemv_nf4(a, dtype == W4A16_BF16, stream));
+  }
+  (void)dev_status;
+  return W4A16_ERR_UNSUPPORTED;
+}
+
+w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                           const int32_t* g_idx, void* W_out, int K, int N, int group_size, w4a16_dtype dtype,
+                           cudaStream_t stream) {
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_int4_shape(0, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(qzeros) || !ok_ptr(W_out)) return W4A16_ERR_INVALID_ARG;
+  if (g_idx && !aligned16(g_idx)) return W4A16_ERR_INVALID_ARG;
+  return from_cuda(launch_dequant_int4(qweight, static_cast<const uint16_t*>(scales), qzeros, g_idx,
+                                       static_cast<uint16_t*>(W_out), K, N, group_size, dtype == W4A16_BF16,
+                                       stream));
+}
+
+w4a16_status nf4_dequant(const uint32_t* qweight, const float* absmax, const float* codebook16, void* W_out, int K,
+                         int N, int blocksize, w4a16_dtype dtype, cudaStream_t stream) {
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_nf4_shape(0, N, K, blocksize);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(codebook16) || !ok_ptr(W_out)) return W4A16_ERR_INVALID_ARG;
+  return from_cuda(launch_dequant_nf4(qweight, absmax, codebook16, static_cast<uint16_t*>(W_out), K, N, blocksize,
+                                      dtype == W4A16_BF16, stream));
+}
+
+w4a16_status w4a16_quantize(const float* W, int K, int N, int group_size, uint32_t* qweight, void* scales,
+                            uint32_t* qzeros, cudaStream_t stream) {
+  w4a16_status st = check_int4_shape(0, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(W) || !ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(qzeros)) return W4A16_ERR_INVALID_ARG;
+  return from_cuda(
+      launch_quantize_rtn(W, K, N, group_size, qweight, static_cast<uint16_t*>(scales), qzeros, stream));
+}
+
+w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const float* codebook16, uint32_t* qweight,
+                          float* absmax, cudaStream_t stream) {
+  w4a16_status st = check_nf4_shape(0, N, K, blocksize);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(W) || !ok_ptr(codebook16) || !ok_ptr(qweight) || !ok_ptr(absmax)) return W4A16_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize_nf4(W, K, N, blocksize, codebook16, qweight, absmax, stream));
+}
+
+size_t w4a16_workspace_bytes(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (M <= W4A16_GEMV_MAX_M) return gemv_plan(M, N, K, kInt4Group).workspace_bytes;
+  return 0;
+}
+
+const char* w4a16_status_string(w4a16_status status) {
+  switch (status) {
+    case W4A16_OK: return "ok";
+    case W4A16_ERR_INVALID_ARG: return "invalid argument (shape, pointer, alignment, dtype or workspace)";
+    case W4A16_ERR_UNSUPPORTED: return "unsupported by this build (group or block size, or shape)";
+    case W4A16_ERR_CUDA: return "CUDA runtime or launch error";
+    case W4A16_ERR_TIMEOUT: return "device-side bounded wait expired";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,214 @@
+// Device helpers shared by the W4A16 / NF4 kernels: inline-PTX wrappers and
+// the exact 4-bit -> fp16 / bf16 dequantization of packed words.
+//
+// Dequantization contract (cloud.tencent.com/developer/article/2726413 §2.1:
+// asymmetric quantization with a stored zero point):
+//     w_hat = RNE_dtype((q - z) * s),   q, z in 0..15, s an fp16 scale.
+// (q - z) * s is exact in fp32 (4-bit integer times an 11-bit significand), so
+// the value is one rounding of the exact product.  The routines below reach
+// that value with packed 16-bit arithmetic on pairs of codes:
+//
+//   fp16: a code is placed in the mantissa of a "magic" fp16 whose ulp is 1
+//         (1024 + q: magic 0x6400 with the code in bits 0..3, or 64 + q:
+//         magic 0x5400 with the code in bits 4..7).  Subtracting the same
+//         magic plus z is exact and gives (q - z); one fp16 multiply by s is
+//         the single IEEE rounding of the exact product.
+//   bf16: the code goes into bits 0..3 of 0x4300 (128 + q); subtracting
+//         128 + z gives (q - z) exactly.  s is split as s = s_hi + s_lo with
+//         s_hi the first 8 significant bits of s (exact in bf16) and s_lo the
+//         remaining <= 3 bits (also exact); t = (q - z) * s_lo is exact (<= 7
+//         bits) and fma(q - z, s_hi, t) rounds the exact (q - z) * s once.
+//
+// A packed word holds the codes of 8 consecutive K rows of one column; pair j
+// (j = 0..3) of a word holds rows (j, j + 4) in its (low, high) halves.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace w4a16 {
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  // (a & mask) | magic
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2_bf16(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Two fp32 values -> packed 16-bit pair (lo in bits 0..15), one RNE each.
+__device__ __forceinline__ uint32_t pack2_rn(float lo, float hi, bool bf16) {
+  uint32_t d;
+  if (bf16)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float lo16_to_f32(uint32_t v, bool bf16) {
+  if (bf16) return __uint_as_float(v << 16);
+  return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float hi16_to_f32(uint32_t v, bool bf16) {
+  if (bf16) return __uint_as_float(v & 0xFFFF0000u);
+  return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+// ---------------------------------------------------------------- INT4, fp16
+// Per-(group, column) constants for the fp16 route; each half of a register
+// may belong to a different (group, column), so act-order can mix them.
+struct DqConstF16 {
+  uint32_t z_lo;  // (1024 + z) in both halves: for pairs 0 and 2
+  uint32_t z_hi;  // (64 + z): for pairs 1 and 3
+  uint32_t s;     // fp16 scale
+};
+
+__device__ __forceinline__ DqConstF16 dq_const_f16(uint32_t z, uint32_t s_bits) {
+  DqConstF16 c;
+  c.z_lo = (0x6400u | z) * 0x00010001u;
+  c.z_hi = (0x5400u | (z << 4)) * 0x00010001u;
+  c.s = (s_bits & 0xFFFFu) * 0x00010001u;
+  return c;
+}
+
+// Two (z, s) per register half: lane 0 for the low element, lane 1 for the high.
+__device__ __forceinline__ DqConstF16 dq_const_f16_2(uint32_t z0, uint32_t s0, uint32_t z1, uint32_t s1) {
+  DqConstF16 c;
+  c.z_lo = (0x6400u | z0) | ((0x6400u | z1) << 16);
+  c.z_hi = (0x5400u | (z0 << 4)) | ((0x5400u | (z1 << 4)) << 16);
+  c.s = (s0 & 0xFFFFu) | (s1 << 16);
+  return c;
+}
+
+// The 8 codes of word w -> 4 fp16 pairs: out[j] = (row j, row j + 4).
+__device__ __forceinline__ void dq_word_f16(uint32_t w, const DqConstF16& c, uint32_t out[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t p0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+  const uint32_t p1 = lop3_and_or(w, 0x00F000F0u, 0x54005400u);
+  const uint32_t p2 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);
+  const uint32_t p3 = lop3_and_or(w8, 0x00F000F0u, 0x54005400u);
+  out[0] = hmul2_f16(hsub2_f16(p0, c.z_lo), c.s);
+  out[1] = hmul2_f16(hsub2_f16(p1, c.z_hi), c.s);
+  out[2] = hmul2_f16(hsub2_f16(p2, c.z_lo), c.s);
+  out[3] = hmul2_f16(hsub2_f16(p3, c.z_hi), c.s);
+}
+
+// Same with a separate constant set per pair (act-order: every row of the word
+// may sit in a different group).
+__device__ __forceinline__ void dq_word_f16_rows(uint32_t w, const DqConstF16 c[4], uint32_t out[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t p0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+  const uint32_t p1 = lop3_and_or(w, 0x00F000F0u, 0x54005400u);
+  const uint32_t p2 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);
+  const uint32_t p3 = lop3_and_or(w8, 0x00F000F0u, 0x54005400u);
+  out[0] = hmul2_f16(hsub2_f16(p0, c[0].z_lo), c[0].s);
+  out[1] = hmul2_f16(hsub2_f16(p1, c[1].z_hi), c[1].s);
+  out[2] = hmul2_f16(hsub2_f16(p2, c[2].z_lo), c[2].s);
+  out[3] = hmul2_f16(hsub2_f16(p3, c[3].z_hi), c[3].s);
+}
+
+// ---------------------------------------------------------------- INT4, bf16
+struct DqConstBF16 {
+  uint32_t z;     // (128 + z) as bf16 in both halves
+  uint32_t s_hi;  // first 8 significant bits of s, bf16
+  uint32_t s_lo;  // s - s_hi, exact in bf16
+};
+
+__device__ __forceinline__ void split_scale_bf16(uint32_t s_bits, uint32_t& hi16, uint32_t& lo16) {
+  const float s = __half2float(__ushort_as_half((unsigned short)(s_bits & 0xFFFFu)));
+  const uint32_t hb = __float_as_uint(s) & 0xFFFF0000u;
+  const float lo = s - __uint_as_float(hb);  // exact: at most 3 significant bits
+  hi16 = hb >> 16;
+  // lo has the sign of s or is zero; giving a zero lo the sign of s keeps
+  // (q - z) == 0 with a negative scale at -0, as the exact product is
+  lo16 = (__float_as_uint(lo) | (__float_as_uint(s) & 0x80000000u)) >> 16;
+}
+
+__device__ __forceinline__ DqConstBF16 dq_const_bf16(uint32_t z, uint32_t s_bits) {
+  DqConstBF16 c;
+  uint32_t hi, lo;
+  split_scale_bf16(s_bits, hi, lo);
+  c.z = (0x4300u | z) * 0x00010001u;
+  c.s_hi = hi * 0x00010001u;
+  c.s_lo = lo * 0x00010001u;
+  return c;
+}
+
+__device__ __forceinline__ DqConstBF16 dq_const_bf16_2(uint32_t z0, uint32_t s0, uint32_t z1, uint32_t s1) {
+  DqConstBF16 c;
+  uint32_t hi0, lo0, hi1, lo1;
+  split_scale_bf16(s0, hi0, lo0);
+  split_scale_bf16(s1, hi1, lo1);
+  c.z = (0x4300u | z0) | ((0x4300u | z1) << 16);
+  c.s_hi = hi0 | (hi1 << 16);
+  c.s_lo = lo0 | (lo1 << 16);
+  return c;
+}
+
+__device__ __forceinline__ uint32_t dq_pair_bf16(uint32_t p, const DqConstBF16& c) {
+  const uint32_t v = hsub2_bf16(p, c.z);   // q - z, exact
+  const uint32_t t = hmul2_bf16(v, c.s_lo);  // exact
+  return hfma2_bf16(v, c.s_hi, t);           // one rounding of (q - z) * s
+}
+
+__device__ __forceinline__ void dq_word_bf16(uint32_t w, const DqConstBF16& c, uint32_t out[4]) {
+  out[0] = dq_pair_bf16(lop3_and_or(w, 0x000F000Fu, 0x43004300u), c);
+  out[1] = dq_pair_bf16(lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u), c);
+  out[2] = dq_pair_bf16(lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u), c);
+  out[3] = dq_pair_bf16(lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u), c);
+}
+
+__device__ __forceinline__ void dq_word_bf16_rows(uint32_t w, const DqConstBF16 c[4], uint32_t out[4]) {
+  out[0] = dq_pair_bf16(lop3_and_or(w, 0x000F000Fu, 0x43004300u), c[0]);
+  out[1] = dq_pair_bf16(lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u), c[1]);
+  out[2] = dq_pair_bf16(lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u), c[2]);
+  out[3] = dq_pair_bf16(lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u), c[3]);
+}
+
+// ---------------------------------------------------------------------- NF4
+// w_hat = RNE_dtype(fl32(C[q] * absmax)): an fp32 product, then one rounding.
+// `cb` is the 16-entry codebook (shared or register copy).
+template <bool BF16>
+__device__ __forceinline__ void dq_word_nf4(uint32_t w, const float* cb, float absmax, uint32_t out[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __fmul_rn(cb[(w >> (4 * j)) & 0xFu], absmax);
+    const float hi = __fmul_rn(cb[(w >> (4 * j + 16)) & 0xFu], absmax);
+    out[j] = pack2_rn(lo, hi, BF16);
+  }
+}
+
+}  // namespace w4a16

@@ -1,0 +1,60 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace w4a16 {
+
+// B300: 148 SMs.  The split-K plan is a pure function of the shape so that the
+// workspace size can be computed on the host without a device query.
+constexpr int kNumSMs = 148;
+
+// ----------------------------------------------------------- split-K GEMV
+constexpr int kGemvThreads = 256;               // 8 warps
+constexpr int kGemvCols = 256;                  // columns per CTA (32 per warp)
+constexpr int kGemvTargetCTAs = kNumSMs * 4;    // CTAs to aim for
+
+struct GemvPlan {
+  int blocks_n;          // CTAs along N
+  int splits;            // CTAs along K
+  int groups_per_split;  // K groups (128 rows) each split covers
+  size_t counters_bytes; // semaphore area at the start of the workspace
+  size_t workspace_bytes;
+};
+
+GemvPlan gemv_plan(int M, int N, int K, int rows_per_group);
+
+struct GemvArgs {
+  const uint16_t* X;
+  const uint32_t* qw;
+  const uint16_t* scales;  // INT4: fp16 scales; unused for NF4
+  const uint32_t* qz;      // INT4 packed zeros
+  const int32_t* g_idx;    // INT4 act-order map or nullptr
+  const float* absmax;     // NF4
+  const float* codebook;   // NF4
+  uint16_t* Y;
+  float* partial;
+  int* counters;
+  int M, N, K;
+  int G;                 // number of K groups of `rows_per_group` rows
+  int groups_per_split;
+  int splits;
+};
+
+cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st);
+cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st);
+
+// ------------------------------------------------------- standalone kernels
+cudaError_t launch_dequant_int4(const uint32_t* qw, const uint16_t* scales, const uint32_t* qz,
+                                const int32_t* g_idx, uint16_t* out, int K, int N, int group_size,
+                                bool bf16, cudaStream_t st);
+cudaError_t launch_dequant_nf4(const uint32_t* qw, const float* absmax, const float* codebook, uint16_t* out,
+                               int K, int N, int blocksize, bool bf16, cudaStream_t st);
+cudaError_t launch_quantize_rtn(const float* W, int K, int N, int group_size, uint32_t* qw, uint16_t* scales,
+                                uint32_t* qz, cudaStream_t st);
+cudaError_t launch_quantize_nf4(const float* W, int K, int N, int blocksize, const float* codebook, uint32_t* qw,
+                                float* absmax, cudaStream_t st);
+
+}  // namespace w4a16

@@ -1,0 +1,157 @@
+/*
+ * w4a16.h -- C ABI of the B300 (sm_103a) library for 4-bit weight-only
+ * quantized linear layers: Y[M,N] = X[M,K] . W_hat[K,N], with W_hat
+ * dequantized on the fly from packed 4-bit codes.
+ *
+ * Two weight formats:
+ *
+ *  INT4 (GPTQ / AWQ checkpoints).  Asymmetric round-to-nearest quantization
+ *    with one fp16 scale and one 4-bit zero point per group of 128 rows along
+ *    K (cloud.tencent.com/developer/article/2726413 §2.1 asymmetric
+ *    quantization stores a zero point; §2.2 group-wise granularity, e.g. 128
+ *    elements per scale; "模型量化实践：GPTQ 与 AWQ 在生产环境的精度与速度权衡"
+ *    §3.1 bits=4, group_size=128, zero_point=True).  An optional act-order map
+ *    g_idx assigns every K row to its group ("GPTQ与bitsandbytes对比" GPTQ
+ *    section, --act-order; same §3.1, desc_act=True).
+ *      W_hat[k,n] = RNE_dtype((q[k,n] - z[g,n]) * s[g,n]),  g = g_idx[k] or k/128
+ *
+ *  NF4 (bitsandbytes).  Codes index a 16-entry normal-float codebook, scaled
+ *    per block of 64 consecutive K rows by an fp32 absmax ("LLM量化技术深度对比:
+ *    GPTQ vs AWQ vs bitsandbytes 2026基准全解析" key-data item 2; "GPTQ、AWQ与
+ *    Bitsandbytes：大模型量化三大技术路径深度对比" §2.3 block-wise NF4).
+ *      W_hat[k,n] = RNE_dtype(fl32(C[q[k,n]] * absmax[k/64, n]))
+ *
+ * Fusing the dequantization into the product -- never writing 16-bit weights
+ * to memory -- is what makes the format fast ("LLM量化技术深度对比" key-data
+ * item 1: the same AWQ weights run 10.9x faster with a fused kernel); the
+ * product is the plain one.
+ *
+ * Tensor layouts (all row-major, contiguous, little-endian):
+ *   X       [M, K]     fp16 or bf16 (the compute dtype)
+ *   Y       [M, N]     same dtype as X
+ *   qweight uint32 [K/8, N]: code of row 8i+j, column n in bits 4j..4j+3 of
+ *                      word [i, n] (8 codes per word, packed along K)
+ *   scales  fp16 [K/128, N]                 (INT4)
+ *   qzeros  uint32 [K/128, N/8]: zero point of column 8c+j in bits 4j.. of
+ *                      word [g, c] (packed along N; the stored value is z)
+ *   g_idx   int32 [K]  row -> group, each value in [0, K/128); NULL means k/128
+ *   absmax  fp32 [K/64, N]                  (NF4)
+ *   codebook16 fp32 [16], ascending         (NF4)
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer is a device pointer owned by the caller.  The library
+ *    allocates and frees nothing and never synchronises; each call is
+ *    enqueued on `stream` and returns as soon as it is enqueued.
+ *  - The return value reports host-side errors only: argument validation
+ *    (nothing is launched) and launch errors.  Faults inside a kernel surface
+ *    at the caller's next synchronisation, as for any CUDA call.
+ *  - Pointers must be 16-byte aligned.  N and K must be multiples of 8;
+ *    K a multiple of the group / block size.
+ *  - M == 0 or N == 0 is a valid empty problem: W4A16_OK, nothing launched.
+ *  - The dtype of X and Y is `dtype`; scales are always fp16, absmax fp32.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, bad dtype */
+  W4A16_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  W4A16_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  W4A16_ERR_TIMEOUT = 4      /* a device-side bounded wait expired (written to dev_status) */
+} w4a16_status;
+
+typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
+
+/* Largest token count the split-K decode kernel (w4a16_gemv) accepts. */
+#define W4A16_GEMV_MAX_M 16
+
+/*
+ * Y = X . W_hat for the INT4 format, any M >= 0.  Dispatches on M: M <= 16
+ * runs the split-K decode kernel (as w4a16_gemv), larger M the tcgen05
+ * tensor-core kernel.
+ *   group_size: 128.
+ *   workspace: device scratch of at least w4a16_workspace_bytes(M, N, K)
+ *     bytes, zero-filled by the caller before its first use; every call that
+ *     completes leaves it zero-filled again.  May be NULL when that size is 0.
+ *     Calls that run at the same time must not share a workspace.
+ *   dev_status: NULL, or a device int the caller zeroes; a kernel whose
+ *     bounded wait expires writes W4A16_ERR_TIMEOUT there and stops early
+ *     (its Y is then undefined).
+ */
+w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scales,
+                        const uint32_t* qzeros, const int32_t* g_idx, void* Y,
+                        int M, int N, int K, int group_size, w4a16_dtype dtype,
+                        void* workspace, size_t workspace_bytes, int* dev_status,
+                        cudaStream_t stream);
+
+/* Y = X . W_hat for the INT4 format and 0 <= M <= W4A16_GEMV_MAX_M: the
+ * weight-streaming decode kernel (split along K, fp32 partial sums reduced
+ * in a fixed order, so results are deterministic).  Arguments as w4a16_gemm. */
+w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scales,
+                        const uint32_t* qzeros, const int32_t* g_idx, void* Y,
+                        int M, int N, int K, int group_size, w4a16_dtype dtype,
+                        void* workspace, size_t workspace_bytes, int* dev_status,
+                        cudaStream_t stream);
+
+/* Y = X . W_hat for the NF4 format, any M >= 0.  blocksize: 64.
+ * codebook16 must not be NULL.  Other arguments as w4a16_gemm. */
+w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absmax,
+                      const float* codebook16, void* Y, int M, int N, int K, int blocksize,
+                      w4a16_dtype dtype, void* workspace, size_t workspace_bytes,
+                      int* dev_status, cudaStream_t stream);
+
+/* W_out[K, N] (dtype) = W_hat, the INT4 dequantization written out; bit-exact
+ * with the definition above.  g_idx may be NULL. */
+w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                           const int32_t* g_idx, void* W_out, int K, int N, int group_size,
+                           w4a16_dtype dtype, cudaStream_t stream);
+
+/* W_out[K, N] (dtype) = W_hat for NF4; bit-exact with the definition above. */
+w4a16_status nf4_dequant(const uint32_t* qweight, const float* absmax, const float* codebook16,
+                         void* W_out, int K, int N, int blocksize, w4a16_dtype dtype,
+                         cudaStream_t stream);
+
+/*
+ * Round-to-nearest INT4 quantization of fp32 W[K, N] with contiguous groups
+ * ("GPTQ与bitsandbytes对比" GPTQ section: RTN is the plain baseline quantizer;
+ * cloud.tencent.com/developer/article/2726413 §2.1-2.2).  Per group g and
+ * column n, in fp64:
+ *   mn = min(min_k w, 0), mx = max(max_k w, 0), s = RNE_fp16((mx - mn) / 15)
+ *   (s = 1 if that is 0), z = clamp(rint(-mn / s), 0, 15),
+ *   q = clamp(rint(w / s) + z, 0, 15)      (rint: half to even)
+ * Outputs qweight [K/8, N], scales fp16 [K/128, N], qzeros [K/128, N/8].
+ */
+w4a16_status w4a16_quantize(const float* W, int K, int N, int group_size, uint32_t* qweight,
+                            void* scales, uint32_t* qzeros, cudaStream_t stream);
+
+/*
+ * NF4 quantization of fp32 W[K, N] ("GPTQ、AWQ与Bitsandbytes" §2.3: block-wise,
+ * calibration-free).  absmax = max |w| over each block of 64 rows of a
+ * column; v = fl32(w / absmax); q = the index of the codebook entry nearest
+ * to v (exact comparison, ties to the lower index; code 7 for an all-zero
+ * block).  Outputs qweight [K/8, N] and absmax fp32 [K/64, N].
+ */
+w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const float* codebook16,
+                          uint32_t* qweight, float* absmax, cudaStream_t stream);
+
+/* Bytes of workspace w4a16_gemm / w4a16_gemv / nf4_gemm need for this
+ * shape (0 when none is needed).  Pure host function. */
+size_t w4a16_workspace_bytes(int M, int N, int K);
+
+/* Static, human-readable text for a status code.  Pure host function. */
+const char* w4a16_status_string(w4a16_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,95 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports every
+function include/w4a16.h declares, and rejects bad arguments before launching
+anything (these calls fail validation, so they never reach the GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:w4a16_status|size_t|const char\*)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import bit_weight_only_wise_b300 as w4
+
+    return w4._lib
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared()
+    for n in ("w4a16_gemm", "w4a16_gemv", "nf4_gemm", "w4a16_dequant", "nf4_dequant", "w4a16_quantize",
+              "nf4_quantize", "w4a16_workspace_bytes", "w4a16_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import bit_weight_only_wise_b300 as w4
+
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in w4.EXPORTED, name
+
+
+def test_status_strings(lib):
+    import bit_weight_only_wise_b300 as w4
+
+    for s in range(5):
+        assert len(w4.status_string(s)) >= 2
+    assert "unknown" in w4.status_string(99)
+
+
+def _gemm(lib, fn="w4a16_gemm", X=16, qw=16, sc=16, qz=16, gi=None, Y=16, M=4, N=64, K=256, g=128, dt=1,
+          ws=None, wsb=0):
+    return getattr(lib, fn)(X, qw, sc, qz, gi, Y, M, N, K, g, dt, ws, wsb, None, None)
+
+
+def test_validation_rejects_without_launch(lib):
+    import bit_weight_only_wise_b300 as w4
+
+    INV, UNS = w4.ERR_INVALID_ARG, w4.ERR_UNSUPPORTED
+    assert _gemm(lib, dt=7) == INV  # dtype
+    assert _gemm(lib, N=60) == INV  # N % 8
+    assert _gemm(lib, K=260) == INV  # K % 8
+    assert _gemm(lib, K=192) == INV  # K % group
+    assert _gemm(lib, K=256, g=64) == UNS  # group size other than 128
+    assert _gemm(lib, K=0) == INV
+    assert _gemm(lib, M=-1) == INV
+    assert _gemm(lib, X=None) == INV  # null pointer
+    assert _gemm(lib, qw=8) == INV  # misaligned (8 bytes)
+    assert _gemm(lib, gi=4) == INV  # misaligned g_idx
+    assert _gemm(lib, fn="w4a16_gemv", M=17) == INV  # decode kernel limit
+    # empty problems are valid no-ops (nothing launched, pointers unused)
+    assert _gemm(lib, M=0, X=None, Y=None) == w4.OK
+    assert _gemm(lib, N=0, X=None, Y=None) == w4.OK
+    # split-K workspace missing or too small
+    need = lib.w4a16_workspace_bytes(4, 64, 256 * 32)
+    if need:
+        assert _gemm(lib, K=256 * 32, ws=None, wsb=0) == INV
+        assert _gemm(lib, K=256 * 32, ws=16, wsb=need - 1) == INV
+    # NF4
+    assert lib.nf4_gemm(16, 16, 16, None, 16, 4, 64, 256, 64, 1, None, 0, None, None) == INV  # codebook
+    assert lib.nf4_gemm(16, 16, 16, 16, 16, 4, 64, 256, 32, 1, None, 0, None, None) == UNS
+    assert lib.nf4_gemm(16, 16, 16, 16, 16, 4, 64, 100, 64, 1, None, 0, None, None) == INV
+    assert lib.w4a16_dequant(16, 16, 16, None, 16, 256, 60, 128, 0, None) == INV
+    assert lib.nf4_dequant(16, 16, None, 16, 256, 64, 64, 0, None) == INV
+    assert lib.w4a16_quantize(None, 256, 64, 128, 16, 16, 16, None) == INV
+    assert lib.nf4_quantize(16, 256, 64, 64, None, 16, 16, None) == INV
+
+
+def test_workspace_sizes_are_pure_and_bounded(lib):
+    assert lib.w4a16_workspace_bytes(0, 4096, 4096) == 0
+    for M in (1, 4, 16):
+        for K, N in ((4096, 4096), (5120, 55296), (27648, 5120), (28672, 8192)):
+            b = lib.w4a16_workspace_bytes(M, N, K)
+            assert b == lib.w4a16_workspace_bytes(M, N, K)
+            assert b <= 64 * 1024 * 1024

@@ -1,0 +1,145 @@
+"""Decode-shape products (M <= 16) through the C ABI against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import bit_weight_only_wise_b300 as w4
+from oracle import int4, nf4, numerics
+from synth import WORKLOADS, act_order_g_idx, activations, gaussian_weights, student_t_weights, weights_for
+
+from gpu_util import (TDT, assert_close, bits, int4_expected, nf4_expected, sample_columns, to_dev, to_dev_u32,
+                      to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _int4_dev(W, g_idx=None):
+    qw, sc, qz, q, z = int4.quantize_packed(W, 128, g_idx)
+    return (to_dev_u32(qw), to_dev(sc), to_dev_u32(qz), None if g_idx is None else to_dev(g_idx)), (q, sc, z)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 8, 9, 15, 16])
+@pytest.mark.parametrize("act", [False, True])
+def test_gemv_small_all_columns(dtype, M, act):
+    # several column tiles plus a ragged tail, several K groups, every output checked
+    K, N = 1536, 776
+    W = student_t_weights(K, N, 5, 0.01, M) if act else gaussian_weights(K, N, 0.02, M)
+    g_idx = act_order_g_idx(K, 128, M) if act else None
+    dev_t, _ = _int4_dev(W, g_idx)
+    X = activations(M, K, dtype, M)
+    Y = w4.gemv(X.cuda(), *dev_t[:3], g_idx=dev_t[3])
+    torch.cuda.synchronize()
+    Y_ref, A = int4_expected(W, X.double().numpy(), dtype, None, g_idx)
+    assert_close(to_f64(Y), Y_ref, A, f"M={M} {dtype} act={act}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("act", [False, True])
+def test_gemv_one_hot_rows_are_exact(dtype, act):
+    # X = rows of the identity: each Y row must equal a row of W_hat bit for bit
+    # (one product by 1.0 per output, then an exact rounding), which pins the
+    # kernel's indexing of rows, columns, groups and the act-order map exactly
+    K, N = 1024, 520
+    W = gaussian_weights(K, N, 0.02, 3)
+    g_idx = act_order_g_idx(K, 128, 3) if act else None
+    dev_t, (q, sc, z) = _int4_dev(W, g_idx)
+    rows = np.array([0, 1, 7, 8, 127, 128, 500, 511, 512, 640, 777, 895, 1000, 1016, 1022, 1023])
+    X = torch.zeros((16, K), dtype=TDT[dtype])
+    X[torch.arange(16), torch.from_numpy(rows)] = 1.0
+    Y = w4.gemv(X.cuda(), *dev_t[:3], g_idx=dev_t[3])
+    w_hat = int4.dequant(q, sc, z, dtype, 128, g_idx)
+    assert np.array_equal(bits(Y), w_hat[rows])
+
+
+def test_gemv_zero_when_codes_equal_zero_points():
+    K, N = 512, 264
+    rng = np.random.default_rng(0)
+    z = rng.integers(0, 16, size=(K // 128, N)).astype(np.uint8)
+    q = z[np.arange(K) // 128]
+    sc = numerics.to_f16(rng.uniform(1e-3, 0.1, size=(K // 128, N)))
+    X = activations(5, K, "bf16", 1).cuda()
+    Y = w4.gemv(X, to_dev_u32(int4.pack_along_k(q)), to_dev(sc), to_dev_u32(int4.pack_zeros(z)))
+    assert torch.count_nonzero(Y.float()).item() == 0
+
+
+def test_gemv_deterministic_and_workspace_reuse():
+    K, N = 4096, 4096
+    W = gaussian_weights(K, N, 0.02, 0)
+    dev_t, _ = _int4_dev(W)
+    X = activations(16, K, "f16", 0).cuda()
+    Y1 = w4.gemv(X, *dev_t[:3])
+    Y2 = w4.gemv(X, *dev_t[:3])
+    Y3 = w4.gemv(X[:3].contiguous(), *dev_t[:3])  # different M through the same workspace
+    Y4 = w4.gemv(X, *dev_t[:3])
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    assert torch.equal(Y1.view(torch.int16), Y4.view(torch.int16))
+    assert torch.equal(Y3.view(torch.int16), Y1[:3].view(torch.int16))
+
+
+def test_gemm_entry_dispatches_small_m_to_gemv():
+    K, N = 1024, 512
+    W = gaussian_weights(K, N, 0.02, 1)
+    dev_t, _ = _int4_dev(W)
+    X = activations(16, K, "bf16", 1).cuda()
+    assert torch.equal(w4.gemm(X, *dev_t[:3]).view(torch.int16), w4.gemv(X, *dev_t[:3]).view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_nf4_gemv_small(dtype, M):
+    K, N = 1024 + 64, 520  # K not a multiple of 128: a half chunk at the end
+    W = gaussian_weights(K, N, 0.02, 7)
+    cb = nf4.codebook()
+    qw, am, _ = nf4.nf4_quantize_packed(W, cb)
+    X = activations(M, K, dtype, 2)
+    Y = w4.nf4_gemm(X.cuda(), to_dev_u32(qw), to_dev(am), to_dev(cb))
+    Y_ref, A = nf4_expected(W, X.double().numpy(), cb, dtype)
+    assert_close(to_f64(Y), Y_ref, A, f"nf4 M={M} {dtype}")
+
+
+def _full_size_cases():
+    out = []
+    for name in ("single_linear", "decode_sweep", "act_order", "qwen32b"):
+        wl = WORKLOADS[name]
+        for (K, N) in wl.shapes:
+            Ms = [m for m in wl.Ms if m <= 16]
+            if Ms:
+                out.append(pytest.param(name, K, N, tuple(Ms), id=f"{name}-{K}x{N}"))
+    return out
+
+
+@pytest.mark.parametrize("name,K,N,Ms", _full_size_cases())
+def test_gemv_full_size_sampled_columns(name, K, N, Ms):
+    # the workloads' full shapes, launched exactly as the bench launches them;
+    # the oracle recomputes a sample of output columns (first, last, random)
+    wl = WORKLOADS[name]
+    W = weights_for(wl, K, N, 0)
+    g_idx = act_order_g_idx(K, 128, 0) if wl.act_order else None
+    cols = sample_columns(N)
+    if g_idx is None:
+        qw, sc, qz = w4.quantize(to_dev(W))
+        qw_o, sc_o, qz_o, _, _ = int4.quantize_packed(W[:, cols])
+        assert np.array_equal(qw.cpu().numpy().view(np.uint32)[:, cols], qw_o)
+        gi = None
+    else:
+        (qw, sc, qz, gi), _ = _int4_dev(W, g_idx)
+    for M in Ms:
+        X = activations(M, K, wl.dtype, M)
+        Y = w4.gemm(X.cuda(), qw, sc, qz, g_idx=gi)
+        Y_ref, A = int4_expected(W, X.double().numpy(), wl.dtype, cols, g_idx)
+        assert_close(to_f64(Y)[:, cols], Y_ref, A, f"{name} {K}x{N} M={M}")
+
+
+def test_nf4_gemv_full_size_sampled_columns():
+    wl = WORKLOADS["nf4"]
+    K, N = wl.shapes[0]
+    W = weights_for(wl, K, N, 0)
+    cb = nf4.codebook()
+    qw, am = w4.nf4_quantize(to_dev(W), to_dev(cb))
+    cols = sample_columns(N)
+    X = activations(1, K, "bf16", 1)
+    Y = w4.nf4_gemm(X.cuda(), qw, am, to_dev(cb))
+    Y_ref, A = nf4_expected(W, X.double().numpy(), cb, "bf16", cols)
+    assert_close(to_f64(Y)[:, cols], Y_ref, A, "nf4 full M=1")
