@@ -27,7 +27,7 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 // Shape checks common to the INT4 entry points.  Returns OK, or the error.
 w4a16_status check_int4_shape(int M, int N, int K, int group_size) {
   if (M < 0 || N < 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
-  if (N % 8 || K % 8 || K > kMaxK) return W4A16_ERR_INVALID_ARG;
+  if (N % 8 || K % 8 || K > kMaxK || N > kMaxColBlocks * kGemvCols) return W4A16_ERR_INVALID_ARG;
   if (group_size <= 0 || K % group_size) return W4A16_ERR_INVALID_ARG;
   if (group_size != kInt4Group) return W4A16_ERR_UNSUPPORTED;
   return W4A16_OK;
@@ -35,7 +35,7 @@ w4a16_status check_int4_shape(int M, int N, int K, int group_size) {
 
 w4a16_status check_nf4_shape(int M, int N, int K, int blocksize) {
   if (M < 0 || N < 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
-  if (N % 8 || K % 8 || K > kMaxK) return W4A16_ERR_INVALID_ARG;
+  if (N % 8 || K % 8 || K > kMaxK || N > kMaxColBlocks * kGemvCols) return W4A16_ERR_INVALID_ARG;
   if (blocksize <= 0 || K % blocksize) return W4A16_ERR_INVALID_ARG;
   if (blocksize != kNF4Block) return W4A16_ERR_UNSUPPORTED;
   return W4A16_OK;
@@ -61,7 +61,7 @@ GemvArgs gemv_args(const void* X, const uint32_t* qw, void* Y, int M, int N, int
   a.splits = p.splits;
   if (p.splits > 1) {
     a.counters = static_cast<int*>(ws);
-    a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + p.counters_bytes);
+    a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kCountersBytes);
   }
   return a;
 }

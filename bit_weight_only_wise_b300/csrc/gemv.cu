@@ -310,8 +310,7 @@ GemvPlan gemv_plan(int M, int N, int K, int rows_per_group) {
   p.groups_per_split = G > 0 ? (G + s - 1) / s : 1;
   p.splits = G > 0 ? (G + p.groups_per_split - 1) / p.groups_per_split : 1;
   if (p.splits > 1 && M > 0) {
-    p.counters_bytes = ((size_t)p.blocks_n * sizeof(int) + 255) / 256 * 256;
-    p.workspace_bytes = p.counters_bytes + (size_t)p.splits * M * N * sizeof(float);
+    p.workspace_bytes = kCountersBytes + (size_t)p.splits * M * N * sizeof(float);
   }
   return p;
 }

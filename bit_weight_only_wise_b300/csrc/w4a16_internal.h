@@ -15,12 +15,17 @@ constexpr int kNumSMs = 148;
 constexpr int kGemvThreads = 256;               // 8 warps
 constexpr int kGemvCols = 256;                  // columns per CTA (32 per warp)
 constexpr int kGemvTargetCTAs = kNumSMs * 4;    // CTAs to aim for
+// The workspace starts with a fixed-size area of split-K tickets (one int per
+// column block) and the fp32 partial sums follow it.  The area's size does not
+// depend on the shape, so partial sums of one call never land where a later
+// call with another shape keeps its tickets.
+constexpr int kMaxColBlocks = 4096;
+constexpr size_t kCountersBytes = kMaxColBlocks * sizeof(int);
 
 struct GemvPlan {
   int blocks_n;          // CTAs along N
   int splits;            // CTAs along K
   int groups_per_split;  // K groups (128 rows) each split covers
-  size_t counters_bytes; // semaphore area at the start of the workspace
   size_t workspace_bytes;
 };
 

@@ -143,3 +143,19 @@ def test_nf4_gemv_full_size_sampled_columns():
     Y = w4.nf4_gemm(X.cuda(), qw, am, to_dev(cb))
     Y_ref, A = nf4_expected(W, X.double().numpy(), cb, "bf16", cols)
     assert_close(to_f64(Y)[:, cols], Y_ref, A, "nf4 full M=1")
+
+
+def test_gemv_workspace_shared_across_shapes():
+    # one cached workspace serves calls whose split-K plans differ; a call must
+    # not find stale partial sums where its tickets live
+    cases = [(1024, 512), (2048, 3072), (1024, 22016), (4096, 776), (1024, 512)]
+    outs = []
+    for K, N in cases:
+        W = gaussian_weights(K, N, 0.02, K + N)
+        dev_t, _ = _int4_dev(W)
+        X = activations(3, K, "bf16", 5)
+        Y = w4.gemv(X.cuda(), *dev_t[:3])
+        Y_ref, A = int4_expected(W, X.double().numpy(), "bf16")
+        assert_close(to_f64(Y), Y_ref, A, f"{K}x{N}")
+        outs.append(Y)
+    assert torch.equal(outs[0].view(torch.int16), outs[-1].view(torch.int16))
