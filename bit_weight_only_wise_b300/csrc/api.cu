@@ -117,8 +117,19 @@ w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scal
   if (M <= W4A16_GEMV_MAX_M)
     return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
                           stream);
-  (void)dev_status;
-  return W4A16_ERR_UNSUPPORTED;
+  if (g_idx) return W4A16_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.X = X;
+  a.qw = qweight;
+  a.scales = static_cast<const uint16_t*>(scales);
+  a.qz = qzeros;
+  a.g_idx = g_idx;
+  a.Y = static_cast<uint16_t*>(Y);
+  a.dev_status = dev_status;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  return from_cuda(launch_gemm_tc(a, dtype == W4A16_BF16, false, stream));
 }
 
 w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absmax, const float* codebook16,
@@ -139,8 +150,17 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
     a.codebook = codebook16;
     return from_cuda(launch_gemv_nf4(a, dtype == W4A16_BF16, stream));
   }
-  (void)dev_status;
-  return W4A16_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.X = X;
+  a.qw = qweight;
+  a.absmax = absmax;
+  a.codebook = codebook16;
+  a.Y = static_cast<uint16_t*>(Y);
+  a.dev_status = dev_status;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  return from_cuda(launch_gemm_tc(a, dtype == W4A16_BF16, true, stream));
 }
 
 w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales, const uint32_t* qzeros,

@@ -198,6 +198,47 @@ __device__ __forceinline__ void dq_word_bf16_rows(uint32_t w, const DqConstBF16 
   out[3] = dq_pair_bf16(lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u), c[3]);
 }
 
+// -------------------------------------------------- natural K order pairs
+// The tensor-memory A operand needs each 32-bit cell to hold two consecutive
+// K rows, (2j, 2j+1).  Byte j of a word holds exactly those two codes; a byte
+// permute copies it into both 16-bit halves and the magic masks pick the low
+// code in the low half and the high code in the high half.
+//   fp16: low half 1024 + q (code in bits 0..3), high half 64 + q (code in
+//         bits 4..7 of that half), so the zero-point constant differs by half.
+//   bf16: the high half takes byte j of (w >> 4), so both codes sit in bits
+//         0..3 of their half under the 128 magic.
+__device__ __forceinline__ uint32_t dq_zmix_f16(uint32_t z) {
+  return (0x6400u | z) | ((0x5400u | (z << 4)) << 16);
+}
+
+__device__ __forceinline__ void dq_word_nat_f16(uint32_t w, uint32_t zmix, uint32_t s2, uint32_t out[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t u = prmt(w, 0u, 0x1111u * j);
+    out[j] = hmul2_f16(hsub2_f16(lop3_and_or(u, 0x00F0000Fu, 0x54006400u), zmix), s2);
+  }
+}
+
+__device__ __forceinline__ void dq_word_nat_bf16(uint32_t w, const DqConstBF16& c, uint32_t out[4]) {
+  const uint32_t w4 = w >> 4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t sel = (uint32_t)j * 0x0011u + (uint32_t)(4 + j) * 0x1100u;
+    const uint32_t u = prmt(w, w4, sel);
+    out[j] = dq_pair_bf16(lop3_and_or(u, 0x000F000Fu, 0x43004300u), c);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void dq_word_nat_nf4(uint32_t w, const float* cb, float absmax, uint32_t out[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __fmul_rn(cb[(w >> (8 * j)) & 0xFu], absmax);
+    const float hi = __fmul_rn(cb[(w >> (8 * j + 4)) & 0xFu], absmax);
+    out[j] = pack2_rn(lo, hi, BF16);
+  }
+}
+
 // ---------------------------------------------------------------------- NF4
 // w_hat = RNE_dtype(fl32(C[q] * absmax)): an fp32 product, then one rounding.
 // `cb` is the 16-entry codebook (shared or register copy).

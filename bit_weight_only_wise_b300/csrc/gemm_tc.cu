@@ -1,0 +1,352 @@
+// Tensor-core kernel for prefill shapes (M > 16): Y[M,N] = X[M,K] . W_hat[K,N]
+// with W_hat dequantized on the fly, on sm_100-family tcgen05 MMAs.
+//
+// Formulation.  The product is computed transposed, D = W_hat^T . X^T, so
+// that the dequantized weights are the MMA's A operand and can live in
+// tensor memory (TMEM): a CTA owns 128 output columns (the MMA's M = 128
+// TMEM lanes, one column per lane) and BT tokens (the MMA's N, 32..256).
+// Dequantizing into TMEM keeps the 16-bit weights off shared memory entirely;
+// X^T is the B operand, staged in shared memory by TMA with 128-byte swizzle
+// (K-major).  The fp32 accumulator D[128 x BT] also lives in TMEM.
+//
+// Pipeline (one CTA, 10 warps):
+//   warp 0     TMA producer: per 64-row K block, the X tile [BT x 64] and the
+//              packed weight tile [8 word-rows x 128 columns] into a ring of
+//              shared-memory stages (mbarrier with transaction count).
+//   warp 1     allocates TMEM; one lane issues the MMAs (4 x K=16 per stage)
+//              and commits them to mbarriers that free the stage and the A
+//              buffer.
+//   warps 2-9  dequantize: thread = one output column (its TMEM lane), each of
+//              the two warps sharing a lane quarter takes 4 of the stage's 8
+//              word-rows; codes -> exact fp16/bf16 pairs in natural K order ->
+//              tcgen05.st into one of 4 A buffers.  After the K loop the same
+//              warps read D back (tcgen05.ld) and write Y.
+//
+// Dequantization follows the pages' format (cloud.tencent.com/developer/
+// article/2726413 §2.1-2.2: asymmetric, one scale and zero point per group of
+// 128 rows); the fusion itself is what "LLM量化技术深度对比:GPTQ vs AWQ vs
+// bitsandbytes 2026基准全解析" key-data item 1 credits for speed.
+//
+// Every mbarrier wait is bounded (see sm100.cuh); on expiry the CTA raises an
+// abort flag, writes W4A16_ERR_TIMEOUT to the caller's status word, waits
+// (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+
+#include "dq_common.cuh"
+#include "sm100.cuh"
+#include "w4a16_internal.h"
+
+namespace w4a16 {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kBN = 128;       // output columns per CTA (MMA M, TMEM lanes)
+constexpr int kBK = 64;        // K rows per stage
+constexpr int kMaxBT = 256;    // tokens per CTA (MMA N)
+constexpr int kStages = 4;
+constexpr int kABufs = 4;
+constexpr int kDqWarps = 8;
+constexpr int kThreads = 32 * (2 + kDqWarps);
+constexpr int kXStageBytes = kMaxBT * kBK * 2;     // 32 KB
+constexpr int kWStageBytes = (kBK / 8) * kBN * 4;  // 4 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemA = 256;  // first A-buffer column; D uses [0, BT)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+struct __align__(8) Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t a_full[kABufs];
+  uint64_t a_empty[kABufs];
+  uint64_t d_full;
+  uint32_t tmem_base;
+  int abort;
+  float cb[16];
+};
+
+constexpr int kSmemBytes = 1024 /* alignment slack */ + kStages * (kXStageBytes + kWStageBytes) + 1024;
+
+struct GemmParams {
+  const uint16_t* scales;
+  const uint32_t* qz;
+  const float* absmax;
+  const float* codebook;
+  uint16_t* Y;
+  int* dev_status;
+  int M, N, K;
+  int BT;
+  uint32_t idesc;
+};
+
+enum { kFmtInt4 = 0, kFmtNF4 = 2 };
+
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sx = smem;                                   // kStages x 32 KB
+  uint32_t* sw = reinterpret_cast<uint32_t*>(smem + kStages * kXStageBytes);  // kStages x 4 KB
+  Bars* bars = reinterpret_cast<Bars*>(smem + kStages * (kXStageBytes + kWStageBytes));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBN;
+  const int m0 = blockIdx.y * p.BT;
+  const int nkb = (p.K + kBK - 1) / kBK;
+  volatile int* abort = &bars->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], kDqWarps + 1);
+    }
+    for (int b = 0; b < kABufs; ++b) {
+      mbar_init(&bars->a_full[b], kDqWarps);
+      mbar_init(&bars->a_empty[b], 1);
+    }
+    mbar_init(&bars->d_full, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  }
+  if (FMT == kFmtNF4 && threadIdx.x < 16) bars->cb[threadIdx.x] = p.codebook[threadIdx.x];
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t tx = (uint32_t)(p.BT * kBK * 2 + kWStageBytes);
+      int issued = 0;
+      for (int it = 0; it < nkb; ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait(&bars->empty[s], ((it / kStages) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) break;
+        mbar_arrive_expect_tx(&bars->full[s], tx);
+        tma_load_2d(sx + s * kXStageBytes, &tmX, &bars->full[s], it * kBK, m0);
+        tma_load_2d(sw + s * (kWStageBytes / 4), &tmW, &bars->full[s], n0, it * (kBK / 8));
+        issued = it + 1;
+      }
+      if (*abort) {
+        // let every copy this CTA started land before its shared memory goes
+        // away: the last phase issued on each stage
+        for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it)
+          (void)mbar_drain(&bars->full[it % kStages], (it / kStages) & 1, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      for (int it = 0; it < nkb; ++it) {
+        const int s = it % kStages;
+        const int b = it % kABufs;
+        if (!mbar_wait(&bars->full[s], (it / kStages) & 1, abort, p.dev_status, kWaitLimitNs)) break;
+        if (!mbar_wait(&bars->a_full[b], (it / kABufs) & 1, abort, p.dev_status, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(sx + s * kXStageBytes));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_ts(tmem, tmem + kTmemA + 32u * b + 8u * kk, bdesc + 2u * kk, p.idesc, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->empty[s]);
+        mma_commit(&bars->a_empty[b]);
+      }
+      mma_commit(&bars->d_full);  // also marks "no MMA in flight" when aborting
+    }
+  } else {
+    // ---------------------------------------------------- dequant + epilogue
+    const int dw = warp - 2;
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int h = dw >> 2;         // which 4 word-rows of a stage
+    const int nl = quarter * 32 + lane;
+    const int n = n0 + nl;
+    const bool ok = n < p.N;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+
+    // per-group constants, with the next group's raw values fetched early
+    uint32_t s_raw = 0, z_raw = 0, s_nxt = 0, z_nxt = 0;
+    float am = 0.f, am_nxt = 0.f;
+    auto fetch = [&](int kb, uint32_t& s_out, uint32_t& z_out, float& am_out) {
+      if (!ok || kb >= nkb) return;
+      if (FMT == kFmtInt4) {
+        const int grp = kb >> 1;  // 128-row groups, 64-row stages
+        s_out = p.scales[(size_t)grp * p.N + n];
+        z_out = (p.qz[(size_t)grp * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu;
+      } else {
+        am_out = p.absmax[(size_t)kb * p.N + n];  // 64-row blocks == stages
+      }
+    };
+    fetch(0, s_raw, z_raw, am);
+    fetch(FMT == kFmtInt4 ? 2 : 1, s_nxt, z_nxt, am_nxt);
+    uint32_t zmix = dq_zmix_f16(z_raw), s2 = s_raw * 0x10001u;
+    DqConstBF16 cbf = dq_const_bf16(z_raw, s_raw);
+
+    bool alive = true;
+    for (int it = 0; it < nkb && alive; ++it) {
+      const int s = it % kStages;
+      const int b = it % kABufs;
+      if (it > 0 && (FMT == kFmtNF4 || (it & 1) == 0)) {
+        s_raw = s_nxt;
+        z_raw = z_nxt;
+        am = am_nxt;
+        fetch(FMT == kFmtInt4 ? it + 2 : it + 1, s_nxt, z_nxt, am_nxt);
+        if (FMT == kFmtInt4) {
+          if (BF16) cbf = dq_const_bf16(z_raw, s_raw);
+          else {
+            zmix = dq_zmix_f16(z_raw);
+            s2 = s_raw * 0x10001u;
+          }
+        }
+      }
+      if (!mbar_wait(&bars->full[s], (it / kStages) & 1, abort, p.dev_status, kWaitLimitNs)) {
+        alive = false;
+        break;
+      }
+      uint32_t wv[4];
+      const uint32_t* wst = sw + s * (kWStageBytes / 4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wv[i] = wst[(4 * h + i) * kBN + nl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->empty[s]);
+      uint32_t regs[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t* o = regs + 4 * i;
+        if (FMT == kFmtNF4) dq_word_nat_nf4<BF16>(wv[i], bars->cb, am, o);
+        else if (BF16) dq_word_nat_bf16(wv[i], cbf, o);
+        else dq_word_nat_f16(wv[i], zmix, s2, o);
+      }
+      if (!mbar_wait(&bars->a_empty[b], ((it / kABufs) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) {
+        alive = false;
+        break;
+      }
+      tmem_st_x16(tmem + lane_off + kTmemA + 32u * b + 16u * h, regs);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->a_full[b]);
+    }
+    __syncwarp();
+
+    // ------------------------------------------------------------ epilogue
+    // d_full is committed even when the CTA aborts, so this also waits for
+    // every MMA in flight before TMEM is freed.
+    const bool done = mbar_drain(&bars->d_full, 0, kDrainLimitNs);
+    tc_fence_after();
+    if (done && !*abort) {
+      const int half = p.BT >> 1;
+      for (int c = h * half; c < (h + 1) * half; c += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tmem + lane_off + (uint32_t)c, v);
+        tmem_wait_ld();
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c + j;
+            if (m < p.M) {
+              const uint32_t y = pack2_rn(__uint_as_float(v[j]), 0.f, BF16);
+              p.Y[(size_t)m * p.N + n] = (uint16_t)(y & 0xFFFFu);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled get_encode() {
+  static PFN_encodeTiled fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled>(ptr);
+  }
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, bool BF16>
+cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const GemmParams& p, dim3 grid,
+                      cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_tc_kernel<FMT, BF16><<<grid, kThreads, kSmemBytes, st>>>(tmX, tmW, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tokens_per_cta(int M) {
+  if (M >= kMaxBT) return kMaxBT;
+  return (M + 31) / 32 * 32;
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st) {
+  const int BT = gemm_tokens_per_cta(a.M);
+  CUtensorMap tmX, tmW;
+  const CUtensorMapDataType xdt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!encode_2d(&tmX, xdt, a.X, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, kBK, (uint32_t)BT,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.qw, (uint64_t)a.N, (uint64_t)(a.K / 8), (uint64_t)a.N * 4,
+                 kBN, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.scales = a.scales;
+  p.qz = a.qz;
+  p.absmax = a.absmax;
+  p.codebook = a.codebook;
+  p.Y = a.Y;
+  p.dev_status = a.dev_status;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.BT = BT;
+  p.idesc = sm100::idesc_f16(bf16, kBN, BT);
+  dim3 grid((a.N + kBN - 1) / kBN, (a.M + BT - 1) / BT);
+  if (nf4) return bf16 ? launch_tc<kFmtNF4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtNF4, false>(tmX, tmW, p, grid, st);
+  return bf16 ? launch_tc<kFmtInt4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtInt4, false>(tmX, tmW, p, grid, st);
+}
+
+}  // namespace w4a16

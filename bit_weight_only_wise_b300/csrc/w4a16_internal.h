@@ -51,6 +51,24 @@ struct GemvArgs {
 cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st);
 cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st);
 
+// ------------------------------------------------------ tensor-core GEMM
+struct GemmArgs {
+  const void* X;
+  const uint32_t* qw;
+  const uint16_t* scales;  // INT4
+  const uint32_t* qz;      // INT4
+  const int32_t* g_idx;    // INT4 act-order map or nullptr
+  const float* absmax;     // NF4
+  const float* codebook;   // NF4
+  uint16_t* Y;
+  int* dev_status;
+  int M, N, K;
+};
+
+// Tokens per CTA (the MMA's N) the tensor-core kernel uses for M tokens.
+int gemm_tokens_per_cta(int M);
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st);
+
 // ------------------------------------------------------- standalone kernels
 cudaError_t launch_dequant_int4(const uint32_t* qw, const uint16_t* scales, const uint32_t* qz,
                                 const int32_t* g_idx, uint16_t* out, int K, int N, int group_size,

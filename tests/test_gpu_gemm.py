@@ -1,0 +1,127 @@
+"""Prefill-shape products (M > 16) on the tcgen05 tensor-core kernel, through
+the C ABI, against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import bit_weight_only_wise_b300 as w4
+from oracle import int4, nf4, numerics, product
+from synth import WORKLOADS, activations, gaussian_weights, student_t_weights, weights_for
+
+from gpu_util import (TDT, assert_close, bits, dev, int4_expected, nf4_expected, sample_columns, to_dev, to_dev_u32,
+                      to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _int4_dev(W, g_idx=None):
+    qw, sc, qz, q, z = int4.quantize_packed(W, 128, g_idx)
+    return (to_dev_u32(qw), to_dev(sc), to_dev_u32(qz), None if g_idx is None else to_dev(g_idx)), (q, sc, z)
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device=dev())
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,K,N", [(17, 256, 128), (32, 256, 264), (64, 1024, 384), (100, 512, 136),
+                                   (256, 1024, 256), (300, 768, 520)])
+def test_gemm_small_all_outputs(dtype, M, K, N):
+    W = gaussian_weights(K, N, 0.02, M + K)
+    dev_t, _ = _int4_dev(W)
+    X = activations(M, K, dtype, M)
+    st = _status()
+    Y = w4.gemm(X.cuda(), *dev_t[:3], dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    Y_ref, A = int4_expected(W, X.double().numpy(), dtype)
+    assert_close(to_f64(Y), Y_ref, A, f"gemm M={M} K={K} N={N} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_gemm_one_hot_rows_are_exact(dtype):
+    K, N = 1024, 264
+    W = student_t_weights(K, N, 5, 0.01, 2)
+    dev_t, (q, sc, z) = _int4_dev(W)
+    rng = np.random.default_rng(0)
+    rows = np.concatenate([[0, 1, 63, 64, 127, 128, 1023], rng.choice(K, 57, replace=False)])
+    M = rows.size
+    X = torch.zeros((M, K), dtype=TDT[dtype])
+    X[torch.arange(M), torch.from_numpy(rows)] = 1.0
+    Y = w4.gemm(X.cuda(), *dev_t[:3])
+    w_hat = int4.dequant(q, sc, z, dtype)
+    assert np.array_equal(bits(Y), w_hat[rows])
+
+
+def test_gemm_zero_when_codes_equal_zero_points():
+    K, N = 512, 256
+    rng = np.random.default_rng(1)
+    z = rng.integers(0, 16, size=(K // 128, N)).astype(np.uint8)
+    q = z[np.arange(K) // 128]
+    sc = numerics.to_f16(rng.uniform(1e-3, 0.1, size=(K // 128, N)))
+    X = activations(64, K, "bf16", 1).cuda()
+    Y = w4.gemm(X, to_dev_u32(int4.pack_along_k(q)), to_dev(sc), to_dev_u32(int4.pack_zeros(z)))
+    assert torch.count_nonzero(Y.float()).item() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M", [64, 300])
+def test_nf4_gemm_small(dtype, M):
+    K, N = 1024 + 64, 264
+    W = gaussian_weights(K, N, 0.02, 9)
+    cb = nf4.codebook()
+    qw, am, _ = nf4.nf4_quantize_packed(W, cb)
+    X = activations(M, K, dtype, 3)
+    Y = w4.nf4_gemm(X.cuda(), to_dev_u32(qw), to_dev(am), to_dev(cb))
+    Y_ref, A = nf4_expected(W, X.double().numpy(), cb, dtype)
+    assert_close(to_f64(Y), Y_ref, A, f"nf4 gemm M={M} {dtype}")
+
+
+def _sample_rows(M, n=64, seed=0):
+    if M <= n:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, M - 1], rng.choice(M, n - 2, replace=False)]))
+
+
+def _full_cases():
+    out = []
+    wl = WORKLOADS["qwen32b"]
+    for (K, N), lab in zip(wl.shapes, wl.labels):
+        out.append(pytest.param("qwen32b", K, N, tuple(m for m in wl.Ms if m > 16), id=f"qwen32b-{lab}"))
+    return out
+
+
+@pytest.mark.parametrize("name,K,N,Ms", _full_cases())
+def test_gemm_full_size_sampled(name, K, N, Ms):
+    # the workload's full shapes and token counts, as the bench launches them;
+    # the oracle recomputes 64 sampled rows x ~200 sampled columns
+    wl = WORKLOADS[name]
+    W = weights_for(wl, K, N, 0)
+    qw, sc, qz = w4.quantize(to_dev(W))
+    cols = sample_columns(N)
+    for M in Ms:
+        X = activations(M, K, wl.dtype, M)
+        st = _status()
+        Y = w4.gemm(X.cuda(), qw, sc, qz, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        rows = _sample_rows(M)
+        Y_ref, A = int4_expected(W, X.double().numpy()[rows], wl.dtype, cols)
+        assert_close(to_f64(Y)[np.ix_(rows, cols)], Y_ref, A, f"{name} {K}x{N} M={M}")
+
+
+def test_nf4_gemm_full_size_sampled():
+    wl = WORKLOADS["nf4"]
+    K, N = wl.shapes[0]
+    W = weights_for(wl, K, N, 0)
+    cb = nf4.codebook()
+    qw, am = w4.nf4_quantize(to_dev(W), to_dev(cb))
+    cols = sample_columns(N)
+    for M in (64, 1024):
+        X = activations(M, K, "bf16", M)
+        Y = w4.nf4_gemm(X.cuda(), qw, am, to_dev(cb))
+        rows = _sample_rows(M)
+        Y_ref, A = nf4_expected(W, X.double().numpy()[rows], cb, "bf16", cols)
+        assert_close(to_f64(Y)[np.ix_(rows, cols)], Y_ref, A, f"nf4 full M={M}")
