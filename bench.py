@@ -1,0 +1,403 @@
+"""Benchmark: W4A16 weight-stream GB/s at M=1 and TFLOP/s at M=4096 on B300.
+
+Workload (Qwen2.5-32B-shaped, INT4 asymmetric, group 128, bf16 activations):
+the four linears of one decoder layer -- qkv 5120->7168, o 5120->5120,
+gate_up 5120->55296, down 27648->5120 -- stacked 64 times.
+
+* decode step (the headline ``value``): one token (M=1) through all 64 x 4
+  linears, i.e. 256 launches of the split-K decode kernel that together stream
+  the stack's 16.21 GB of packed weights, scales and zeros.  Timed as CUDA-graph
+  replays with CUDA events; value = weight bytes / time (GB/s).
+* prefill step (``prefill``): M=4096 tokens through one layer's 4 linears on the
+  tcgen05 kernel (a different layer each step); TFLOP/s = 2*M*N*K / time.
+
+Every input is synthetic and seeded: weights W ~ N(0, 0.02) drawn by the
+shared generators, quantized on the GPU by the library's round-to-nearest
+kernel; the 64 layers are 64 distinct device copies of those four quantized
+linears (16.2 GB, far larger than the 126 MB L2, so no L2 flush is needed).
+
+``--impl reference`` times the CPU oracle instead (dequantize + fp64 product)
+on a bounded sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+LINEARS = (("qkv", 5120, 7168), ("o", 5120, 5120), ("gate_up", 5120, 55296), ("down", 27648, 5120))
+LAYERS = 64
+GROUP = 128
+M_PREFILL = 4096
+METRIC = "W4A16 M=1 weight-stream GB/s (Qwen2.5-32B-shaped 64-layer INT4 g128 stack)"
+
+
+def int4_bytes(K, N):
+    G = K // GROUP
+    return K * N // 2 + G * N * 2 + G * N // 2
+
+
+STACK_BYTES = LAYERS * sum(int4_bytes(K, N) for _, K, N in LINEARS)
+LAYER_FLOPS = sum(2 * M_PREFILL * K * N for _, K, N in LINEARS)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a timed region."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        q = "clocks.sm,clocks.max.sm,power.draw," + ",".join("clocks_event_reasons." + r for r in _REASONS)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 3 + len(_REASONS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(_REASONS, f[3:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(seconds: float = 12.0):
+    """Oracle (dequantize + fp64 product) on the o projection at M=1, repeated
+    for about ``seconds``; returns (GB/s of packed weight bytes, cores, sample)."""
+    from oracle import int4, product
+    from synth import activations, gaussian_weights
+
+    K, N = 5120, 5120
+    W = gaussian_weights(K, N, 0.02, 0)
+    q, s, z = int4.rtn_quantize(W)
+    X = activations(1, K, "bf16", 1).double().numpy()
+    nbytes = int4_bytes(K, N)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        w_hat = int4.dequant(q, s, z, "bf16")
+        wf = (w_hat.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        product.reference(X, wf)
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = 1
+    return nbytes * done / dt / 1e9, cores, f"o_proj 5120x5120 INT4 at M=1, {done} passes in {dt:.1f} s"
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    steps, warm = args.steps, args.warmup
+    per = max(2.0, 60.0 / max(1, steps + warm))
+    for _ in range(warm):
+        oracle_sample(per / 2)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        v, cores, sample = oracle_sample(per)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": round(wall * 1e3 / steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "CPU oracle (RTN INT4 dequantize + fp64 product), bounded sample of the "
+                               "Qwen2.5-32B-shaped decode stack", "sample": sample},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- GPU
+def traffic_from_profiles(kernel_src: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current source of the kernel; else None."""
+    import hashlib
+
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = open(os.path.join(ROOT, "bit_weight_only_wise_b300", "csrc", kernel_src), "rb").read()
+    ent = d.get(kernel_src)
+    if not ent or ent.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    return ent
+
+
+def run_gpu(args):
+    import torch
+
+    import bit_weight_only_wise_b300 as w4
+    from synth import activations, gaussian_weights
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm_peak, tc_peak, tc_sustained, peak_src = load_peaks()
+
+    # ---- weights: four linears quantized on the GPU, 64 distinct copies
+    base = []
+    for i, (name, K, N) in enumerate(LINEARS):
+        W = torch.from_numpy(gaussian_weights(K, N, 0.02, 100 + i)).to(dev)
+        base.append(w4.quantize(W))
+        del W
+    torch.cuda.synchronize()
+    stack = [[tuple(t.clone() for t in base[i]) for i in range(4)] for _ in range(LAYERS)]
+    del base
+    torch.cuda.synchronize()
+
+    # ---- decode (M = 1): 256 launches per step, captured once in a graph
+    xs = [activations(1, K, "bf16", 7 + i).to(dev) for i, (_, K, _) in enumerate(LINEARS)]
+    ys = [torch.empty((1, N), dtype=torch.bfloat16, device=dev) for (_, _, N) in LINEARS]
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        wss = [w4.workspace(1, N, K, dev) for (_, K, N) in LINEARS]
+        ws = max(wss, key=lambda t: -1 if t is None else t.numel())
+
+        def decode_step():
+            for layer in stack:
+                for i in range(4):
+                    w4.gemv(xs[i], *layer[i], out=ys[i], ws=ws)
+
+        decode_step()  # attribute setup, first-call work
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            decode_step()
+    torch.cuda.synchronize()
+
+    def timed(fn, steps, warm, stream):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ms = e0.elapsed_time(e1)
+        if dist:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = t.item()
+        return ms
+
+    cur = torch.cuda.current_stream(dev)
+    with ClockSampler(local) as clk:
+        dec_ms = timed(g.replay, args.steps, args.warmup, cur)
+    clocks = clk.summary()
+    dec_step_ms = dec_ms / args.steps
+    value = world * STACK_BYTES * args.steps / (dec_ms * 1e-3) / 1e9
+    per_gpu = STACK_BYTES / (dec_step_ms * 1e-3) / 1e9
+    launches = args.steps * LAYERS * 4
+
+    # ---- e2e: through the API call by call, X from pinned host memory each
+    # step and every output read back
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
+    h2d = sum(x.numel() * x.element_size() for x in xh)
+    d2h = sum(y.numel() * y.element_size() for y in yh)
+
+    def e2e_step():
+        for i in range(4):
+            xs[i].copy_(xh[i], non_blocking=True)
+        decode_step()
+        for i in range(4):
+            yh[i].copy_(ys[i], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(s):
+        e2e_ms = timed(e2e_step, e2e_steps, max(args.warmup, 3), s)
+    e2e_val = world * STACK_BYTES * e2e_steps / (e2e_ms * 1e-3) / 1e9
+
+    # ---- prefill (M = 4096): one layer's four linears per step
+    xp = [activations(M_PREFILL, K, "bf16", 11 + i).to(dev) for i, (_, K, _) in enumerate(LINEARS)]
+    yp = [torch.empty((M_PREFILL, N), dtype=torch.bfloat16, device=dev) for (_, _, N) in LINEARS]
+    pre_state = {"layer": 0}
+    lin_ms = [0.0] * 4
+
+    def prefill_step(record=False):
+        layer = stack[pre_state["layer"] % LAYERS]
+        pre_state["layer"] += 1
+        for i in range(4):
+            w4.gemm(xp[i], *layer[i], out=yp[i])
+
+    pre_steps = max(3, min(args.steps, 20))
+    pre_ms = timed(prefill_step, pre_steps, max(args.warmup, 3), cur)
+    tflops = world * LAYER_FLOPS * pre_steps / (pre_ms * 1e-3) / 1e12
+    # per-linear times (events around each linear, for the roofline of the kernel)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        layer = stack[(rep * 7) % LAYERS]
+        for i in range(4):
+            evs[i][0].record(cur)
+            w4.gemm(xp[i], *layer[i], out=yp[i])
+            evs[i][1].record(cur)
+        torch.cuda.synchronize()
+        for i in range(4):
+            lin_ms[i] += evs[i][0].elapsed_time(evs[i][1]) / 3
+    gate = 2 * M_PREFILL * 5120 * 55296 / (lin_ms[2] * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = oracle_sample(args.cpu_seconds)
+        cpu = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    traffic = traffic_from_profiles("gemv.cu")
+    achieved = per_gpu  # algorithmic bytes per launch / mean launch time == stack bytes / step time
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dec_step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, RTN INT4 g128 on the GPU; N(0,1) bf16 activations)",
+        "config": {
+            "workload": "Qwen2.5-32B-shaped decode: M=1 through 64 layers x {qkv 5120x7168, o 5120x5120, "
+                        "gate_up 5120x55296, down 27648x5120}, INT4 asymmetric g128, bf16 X/Y",
+            "stack_bytes": STACK_BYTES,
+            "launches_per_step": LAYERS * 4,
+            "timing": "CUDA graph replay of the 256 launches, CUDA events; inputs (16.2 GB) larger than L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4),
+            "peak_source": peak_src,
+            "traffic": None if traffic is None else traffic.get("bytes_per_launch"),
+            "kernel": "gemv_kernel (split-K decode)",
+            "algorithmic_bytes_per_launch": STACK_BYTES // (LAYERS * 4),
+        },
+        "prefill": {
+            "metric": "W4A16 M=4096 TFLOP/s (one Qwen2.5-32B-shaped layer, 4 linears)",
+            "value": round(tflops, 1),
+            "unit": "TFLOP/s",
+            "ms_per_step": round(pre_ms / pre_steps, 3),
+            "per_linear_ms": {n: round(t, 4) for (n, _, _), t in zip(LINEARS, lin_ms)},
+            "roofline": {"bound": "tensor", "achieved": round(gate, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": round(gate / tc_peak, 4), "peak_source": peak_src,
+                         "frac_of_sustained": round(gate / tc_sustained, 4) if tc_sustained else None,
+                         "kernel": "gemm_tc_kernel on gate_up 5120x55296"},
+            "layer_frac_of_peak": round(tflops / world / tc_peak, 4),
+        },
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "per step: pinned-host X -> device, 256 C-ABI calls through the Python binding, "
+                       "outputs -> pinned host"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -48,31 +48,30 @@ w4a16_status check_workspace(const GemvPlan& p, void* ws, size_t ws_bytes) {
 }
 
 GemvArgs gemv_args(const void* X, const uint32_t* qw, void* Y, int M, int N, int K, const GemvPlan& p,
-                   void* ws) {
+                   void* ws, int* dev_status) {
   GemvArgs a{};
   a.X = static_cast<const uint16_t*>(X);
   a.qw = qw;
   a.Y = static_cast<uint16_t*>(Y);
+  a.dev_status = dev_status;
   a.M = M;
   a.N = N;
   a.K = K;
-  a.G = (K + 127) / 128;
-  a.groups_per_split = p.groups_per_split;
-  a.splits = p.splits;
-  if (p.splits > 1) {
-    a.counters = static_cast<int*>(ws);
-    a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kCountersBytes);
-  }
+  a.G = p.G;
+  a.blocks_n = p.blocks_n;
+  a.ctas = p.ctas;
+  a.counters = static_cast<int*>(ws);
+  a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kCountersBytes);
   return a;
 }
 
 w4a16_status int4_gemv_impl(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
                             const int32_t* g_idx, void* Y, int M, int N, int K, w4a16_dtype dtype,
-                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  const GemvPlan p = gemv_plan(M, N, K, kInt4Group);
+                            void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  const GemvPlan p = gemv_plan(M, N, K, g_idx ? kInt4Act : kInt4);
   w4a16_status st = check_workspace(p, workspace, workspace_bytes);
   if (st != W4A16_OK) return st;
-  GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace);
+  GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace, dev_status);
   a.scales = static_cast<const uint16_t*>(scales);
   a.qz = qzeros;
   a.g_idx = g_idx;
@@ -94,7 +93,6 @@ extern "C" {
 w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
                         const int32_t* g_idx, void* Y, int M, int N, int K, int group_size, w4a16_dtype dtype,
                         void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
-  (void)dev_status;
   if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
   w4a16_status st = check_int4_shape(M, N, K, group_size);
   if (st != W4A16_OK) return st;
@@ -102,7 +100,8 @@ w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scal
   if (M == 0 || N == 0) return W4A16_OK;
   st = check_int4_ptrs(X, qweight, scales, qzeros, g_idx, Y);
   if (st != W4A16_OK) return st;
-  return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes, stream);
+  return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
+                        dev_status, stream);
 }
 
 w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
@@ -116,7 +115,7 @@ w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scal
   if (st != W4A16_OK) return st;
   if (M <= W4A16_GEMV_MAX_M)
     return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
-                          stream);
+                          dev_status, stream);
   if (g_idx) return W4A16_ERR_UNSUPPORTED;
   GemmArgs a{};
   a.X = X;
@@ -142,10 +141,10 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
   if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(codebook16) || !ok_ptr(Y))
     return W4A16_ERR_INVALID_ARG;
   if (M <= W4A16_GEMV_MAX_M) {
-    const GemvPlan p = gemv_plan(M, N, K, kNF4Block);
+    const GemvPlan p = gemv_plan(M, N, K, kNF4);
     st = check_workspace(p, workspace, workspace_bytes);
     if (st != W4A16_OK) return st;
-    GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace);
+    GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace, dev_status);
     a.absmax = absmax;
     a.codebook = codebook16;
     return from_cuda(launch_gemv_nf4(a, dtype == W4A16_BF16, stream));
@@ -209,7 +208,7 @@ w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const flo
 
 size_t w4a16_workspace_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  if (M <= W4A16_GEMV_MAX_M) return gemv_plan(M, N, K, kInt4Group).workspace_bytes;
+  if (M <= W4A16_GEMV_MAX_M) return gemv_plan(M, N, K, kInt4).workspace_bytes;
   return 0;
 }
 

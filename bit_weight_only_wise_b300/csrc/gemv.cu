@@ -7,37 +7,53 @@
 // item 3: 16 GB of 4-bit weights vs 64 GB at FP16 per forward; item 1: the
 // fused kernel that never writes 16-bit weights is the fast one).
 //
-// Work split.  A CTA (8 warps) owns 256 consecutive output columns and a
-// contiguous range of K groups (128 rows each); a warp owns 32 columns.  Per
-// group, lane (g = lane/4, c = lane%4) loads the 16-byte vectors holding
-// columns [4g, 4g+4) of the packed word-rows c, c+4, c+8, c+12 of the group
-// (128-bit coalesced loads, 512 contiguous bytes per warp and word-row),
-// dequantizes them in registers to exact fp16/bf16 pairs, and feeds them to
-// the tensor cores as the A operand of m16n8k16 MMAs, with the weights' output
-// columns as the MMA's M dimension and the (up to 16) tokens as its N
-// dimension (fp32 accumulation).  The MMA needs matching K orderings for A
-// and B, not the natural one: each lane's pair j = rows (j, j+4) of its word
-// is paired with the activations of the same two rows.
+// Work split (stream-K).  The work is cut into units of 256 output columns x
+// one 128-row K group (16 KB of packed weights).  A persistent grid of
+// 148 x (2 to 4) CTAs takes contiguous, equal-sized ranges of the units in
+// column-block-major order, so every SM streams the same number of bytes
+// whatever the shape.  Inside a CTA each of the 8 warps owns a 32-column slice
+// of the unit and runs its own TMA ring: lane 0 keeps 2-3 2-KB tiles
+// (16 word-rows x 32 columns, 128-byte swizzle) in flight into the warp's
+// shared-memory stages, signalled by per-stage mbarriers; no registers are
+// spent on prefetching and no CTA-wide synchronisation is needed.
 //
-// Split-K reduction.  With more than one split, each CTA writes its fp32
-// partial tile to the workspace, and the last CTA to arrive for a column block
-// (an atomic ticket) sums the splits in index order -- so the result does not
-// depend on arrival order -- rounds once to the output dtype and resets the
-// ticket to zero for the next call.
+// Inner product.  Lane (g = lane/4, c = lane%4) reads, per unit, four 16-byte
+// vectors (columns [4g, 4g+4) of word-rows 2c, 2c+8, 2c+1, 2c+9 -- an order
+// that makes the swizzled reads bank-conflict free), dequantizes them in
+// registers to exact fp16/bf16 pairs and feeds them to m16n8k16 tensor-core
+// MMAs as the A operand, the output columns being the MMA's M dimension and
+// the (up to 16) tokens its N dimension (fp32 accumulation).  The MMA only
+// needs the same K order in A and B: each lane's pair j = rows (j, j+4) of a
+// word meets the activations of the same two rows.
+//
+// Reduction.  A column block covered by one CTA is written directly.  A block
+// shared by several CTAs (at most the first and last block of each range) is
+// reduced through the workspace: each contributor writes its fp32 partial
+// slice and takes a ticket; the last one sums the partials in contributor
+// order -- deterministic whatever the arrival order -- rounds once, and resets
+// the ticket for the next call.
+#include <cuda.h>
+
 #include "dq_common.cuh"
+#include "sm100.cuh"
 #include "w4a16_internal.h"
 
 namespace w4a16 {
 
-enum GemvFmt { kInt4 = 0, kInt4Act = 1, kNF4 = 2 };
+using namespace sm100;
 
-__device__ __forceinline__ uint4 ldg_stream_v4(const uint32_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+namespace {
+
+
+constexpr int kWarps = kGemvThreads / 32;  // 8 column slices per CTA
+constexpr int kTileBytes = 16 * 32 * 4;    // 16 word-rows x 32 columns
+// TMA stages per warp.  Measured on B300: streaming 2-KB boxes runs at ~82%
+// of the copy bandwidth with about 48 copies outstanding per SM (3 CTAs x 8
+// warps x 2, or 2 x 8 x 3); twice as many outstanding copies halve the rate.
+template <int NT>
+constexpr int ring_depth() { return NT == 1 ? 2 : 3; }
+constexpr int gemv_smem(int ring) { return 1024 + kWarps * ring * kTileBytes; }
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 template <bool BF16>
 __device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
@@ -55,263 +71,444 @@ __device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint3
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Dequantize the 4 words (4 columns) of one word-row into pr[column][pair].
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The word-row of the 16-row tile that lane quarter-index c reads at step o.
+__device__ __forceinline__ int tile_row(int c, int o) { return 2 * c + 8 * (o & 1) + (o >> 1); }
+
+// ------------------------------------------------------------- dequantizers
+// fetch(): raw constants of a unit, one unit ahead; begin(): turn them into
+// the current unit's constants; word(): dequantize the word of column
+// col0 + c4 at step o into 4 pairs (rows (j, j+4) of that word-row).
 template <int FMT, bool BF16>
-struct Dequantizer;
+struct Dq;
 
 template <bool BF16>
-struct Dequantizer<kInt4, BF16> {
-  // constants of the 4 columns for the current group
+struct Dq<kInt4, BF16> {
+  // Lane L of the warp owns column L of the 32-column slice: it fetches that
+  // column's scale and zero one unit ahead, turns them into the three packed
+  // constants and publishes them in the warp's shared-memory table; each lane
+  // then reads the constants of its four columns with three 16-byte loads.
+  uint32_t* tab;  // [2 buffers][3][32] words, per warp
+  uint32_t s_nxt, z_nxt;
   DqConstF16 cf[4];
   DqConstBF16 cb[4];
-  __device__ __forceinline__ void load_group(const GemvArgs& a, int gi, int col0, bool ok) {
-    uint2 sv = make_uint2(0, 0);
-    uint32_t zw = 0;
-    if (ok) {
-      sv = __ldg(reinterpret_cast<const uint2*>(a.scales + (size_t)gi * a.N + col0));
-      zw = __ldg(a.qz + (size_t)gi * (a.N >> 3) + (col0 >> 3)) >> (4 * (col0 & 7));
-    }
-    const uint32_t sb[4] = {sv.x & 0xFFFFu, sv.x >> 16, sv.y & 0xFFFFu, sv.y >> 16};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t z = (zw >> (4 * c)) & 0xFu;
-      if (BF16) cb[c] = dq_const_bf16(z, sb[c]);
-      else cf[c] = dq_const_f16(z, sb[c]);
+  int buf = 0;
+  __device__ __forceinline__ void fetch(const GemvArgs& a, int g, int slice0, int lane) {
+    const int n = slice0 + lane;
+    if (n < a.N) {
+      s_nxt = __ldg(a.scales + (size_t)g * a.N + n);
+      z_nxt = (__ldg(a.qz + (size_t)g * (a.N >> 3) + (n >> 3)) >> (4 * (n & 7))) & 0xFu;
+    } else {
+      s_nxt = z_nxt = 0;
     }
   }
-  __device__ __forceinline__ void word_row(const GemvArgs&, const uint4& w, int, int, bool, uint32_t pr[4][4]) {
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  // publish the fetched constants (call before the warp's __syncwarp), ...
+  __device__ __forceinline__ void publish(int lane) {
+    uint32_t* t = tab + buf * 96;
+    if (BF16) {
+      const DqConstBF16 k = dq_const_bf16(z_nxt, s_nxt);
+      t[lane] = k.z;
+      t[32 + lane] = k.s_hi;
+      t[64 + lane] = k.s_lo;
+    } else {
+      const DqConstF16 k = dq_const_f16(z_nxt, s_nxt);
+      t[lane] = k.z_lo;
+      t[32 + lane] = k.z_hi;
+      t[64 + lane] = k.s;
+    }
+  }
+  // ... and read this lane's four columns (after it)
+  __device__ __forceinline__ void begin(int gl) {
+    const uint32_t* t = tab + buf * 96;
+    const uint4 v0 = *reinterpret_cast<const uint4*>(t + 4 * gl);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(t + 32 + 4 * gl);
+    const uint4 v2 = *reinterpret_cast<const uint4*>(t + 64 + 4 * gl);
+    const uint32_t a0[4] = {v0.x, v0.y, v0.z, v0.w}, a1[4] = {v1.x, v1.y, v1.z, v1.w},
+                   a2[4] = {v2.x, v2.y, v2.z, v2.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      if (BF16) dq_word_bf16(ws[c], cb[c], pr[c]);
-      else dq_word_f16(ws[c], cf[c], pr[c]);
+      if (BF16) cb[c] = DqConstBF16{a0[c], a1[c], a2[c]};
+      else cf[c] = DqConstF16{a0[c], a1[c], a2[c]};
     }
+    buf ^= 1;
+  }
+  __device__ __forceinline__ void word(const GemvArgs&, int, uint32_t w, int c4, int, int, bool, uint32_t out[4]) {
+    if (BF16) dq_word_bf16(w, cb[c4], out);
+    else dq_word_f16(w, cf[c4], out);
   }
 };
 
 template <bool BF16>
-struct Dequantizer<kInt4Act, BF16> {
-  __device__ __forceinline__ void load_group(const GemvArgs&, int, int, bool) {}
-  // row0: first K row of the word-row; every row has its own group
-  __device__ __forceinline__ void word_row(const GemvArgs& a, const uint4& w, int row0, int col0, bool ok,
-                                           uint32_t pr[4][4]) {
-    uint32_t sv[8][2], zw[8];
+struct Dq<kInt4Act, BF16> {
+  uint32_t* tab;
+  __device__ __forceinline__ void fetch(const GemvArgs&, int, int, int) {}
+  __device__ __forceinline__ void publish(int) {}
+  __device__ __forceinline__ void begin(int) {}
+  // every row of the word-row sits in its own group
+  __device__ __forceinline__ void word(const GemvArgs& a, int, uint32_t w, int c4, int row0, int col0, bool ok,
+                                       uint32_t out[4]) {
+    uint32_t z[8], s[8];
     if (ok) {
       const int4 g0 = __ldg(reinterpret_cast<const int4*>(a.g_idx + row0));
       const int4 g1 = __ldg(reinterpret_cast<const int4*>(a.g_idx + row0 + 4));
       const int gr[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const int col = col0 + c4;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const uint2 s2 = __ldg(reinterpret_cast<const uint2*>(a.scales + (size_t)gr[r] * a.N + col0));
-        sv[r][0] = s2.x;
-        sv[r][1] = s2.y;
-        zw[r] = __ldg(a.qz + (size_t)gr[r] * (a.N >> 3) + (col0 >> 3)) >> (4 * (col0 & 7));
+        s[r] = __ldg(a.scales + (size_t)gr[r] * a.N + col);
+        z[r] = (__ldg(a.qz + (size_t)gr[r] * (a.N >> 3) + (col >> 3)) >> (4 * (col & 7))) & 0xFu;
       }
     } else {
 #pragma unroll
-      for (int r = 0; r < 8; ++r) sv[r][0] = sv[r][1] = zw[r] = 0;
+      for (int r = 0; r < 8; ++r) s[r] = z[r] = 0;
     }
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if (BF16) {
+      DqConstBF16 k[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t z[8], s[8];
+      for (int j = 0; j < 4; ++j) k[j] = dq_const_bf16_2(z[j], s[j], z[j + 4], s[j + 4]);
+      dq_word_bf16_rows(w, k, out);
+    } else {
+      DqConstF16 k[4];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        z[r] = (zw[r] >> (4 * c)) & 0xFu;
-        s[r] = (sv[r][c >> 1] >> (16 * (c & 1))) & 0xFFFFu;
-      }
-      if (BF16) {
-        DqConstBF16 k[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) k[j] = dq_const_bf16_2(z[j], s[j], z[j + 4], s[j + 4]);
-        dq_word_bf16_rows(ws[c], k, pr[c]);
-      } else {
-        DqConstF16 k[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) k[j] = dq_const_f16_2(z[j], s[j], z[j + 4], s[j + 4]);
-        dq_word_f16_rows(ws[c], k, pr[c]);
-      }
+      for (int j = 0; j < 4; ++j) k[j] = dq_const_f16_2(z[j], s[j], z[j + 4], s[j + 4]);
+      dq_word_f16_rows(w, k, out);
     }
   }
 };
 
 template <bool BF16>
-struct Dequantizer<kNF4, BF16> {
+struct Dq<kNF4, BF16> {
+  uint32_t* tab;
   const float* cbk;  // shared-memory codebook
-  __device__ __forceinline__ void load_group(const GemvArgs&, int, int, bool) {}
-  __device__ __forceinline__ void word_row(const GemvArgs& a, const uint4& w, int row0, int col0, bool ok,
-                                           uint32_t pr[4][4]) {
-    float4 am = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ok && row0 < a.K) am = __ldg(reinterpret_cast<const float4*>(a.absmax + (size_t)(row0 >> 6) * a.N + col0));
-    dq_word_nf4<BF16>(w.x, cbk, am.x, pr[0]);
-    dq_word_nf4<BF16>(w.y, cbk, am.y, pr[1]);
-    dq_word_nf4<BF16>(w.z, cbk, am.z, pr[2]);
-    dq_word_nf4<BF16>(w.w, cbk, am.w, pr[3]);
+  float4 am_nxt[2];  // absmax of the unit's two 64-row blocks, one unit ahead
+  float4 am[2];
+  int gl4;           // first of this lane's four columns, within the slice
+  __device__ __forceinline__ void fetch(const GemvArgs& a, int g, int slice0, int) {
+    const int col0 = slice0 + gl4;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int blk = 2 * g + h;
+      am_nxt[h] = (col0 < a.N && 64 * blk < a.K)
+                      ? __ldg(reinterpret_cast<const float4*>(a.absmax + (size_t)blk * a.N + col0))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __device__ __forceinline__ void publish(int) {}
+  __device__ __forceinline__ void begin(int) {
+    am[0] = am_nxt[0];
+    am[1] = am_nxt[1];
+  }
+  __device__ __forceinline__ void word(const GemvArgs&, int o, uint32_t w, int c4, int, int, bool,
+                                       uint32_t out[4]) {
+    const float4 v = am[o & 1];  // tile rows 0..7 lie in block 0, rows 8..15 in block 1
+    const float amc = c4 == 0 ? v.x : c4 == 1 ? v.y : c4 == 2 ? v.z : v.w;
+    dq_word_nf4<BF16>(w, cbk, amc, out);
   }
 };
 
+// ------------------------------------------------------------ stream-K plan
+struct Range {
+  long long U;  // units
+  int P;        // CTAs
+  __device__ __forceinline__ long long start(int i) const { return U * i / P; }
+  // the CTA whose range holds unit u: the largest i with start(i) <= u
+  __device__ __forceinline__ int owner(long long u) const { return (int)(((u + 1) * P - 1) / U); }
+};
+
 template <int NT, int FMT, bool BF16>
-__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 16, FMT))
+    gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+  constexpr int kRing = ring_depth<NT>();
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kWarps][kRing];
   __shared__ float s_cb[16];
-  __shared__ int s_last;
+  __shared__ __align__(16) uint32_t s_tab[kWarps][2 * 96];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int g = lane >> 2, c = lane & 3;
-  const int col_blk = blockIdx.x * kGemvCols;
-  const int col0 = col_blk + warp * 32 + 4 * g;
-  const bool col_ok = col0 < a.N;
-  const int split = blockIdx.y;
-  const int g_begin = split * a.groups_per_split;
-  const int g_end = min(a.G, g_begin + a.groups_per_split);
-  const size_t N = (size_t)a.N;
+  const int gl = lane >> 2, c = lane & 3;
+  uint8_t* ring = smem + warp * (kRing * kTileBytes);
+  uint64_t* bar = full[warp];
+  volatile int abort_flag = 0;  // per-warp pipeline: nobody else raises it
 
-  Dequantizer<FMT, BF16> dq;
+  const Range R{(long long)a.blocks_n * a.G, (int)gridDim.x};
+  const int cta = blockIdx.x;
+  const long long u0 = R.start(cta);
+  const int nu = (int)(R.start(cta + 1) - u0);
+  const int first_block = (int)(u0 / a.G);
+
+  Dq<FMT, BF16> dq;
+  dq.tab = s_tab[warp];
   if constexpr (FMT == kNF4) {
+    dq.gl4 = 4 * gl;
     if (threadIdx.x < 16) s_cb[threadIdx.x] = a.codebook[threadIdx.x];
     __syncthreads();
     dq.cbk = s_cb;
   }
+  if (lane == 0) {
+    for (int s = 0; s < kRing; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
 
-  float acc[NT][2][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[t][r][i] = 0.f;
-
-  // weights of the next group are loaded while the current one is consumed
-  uint4 wq[4], wn[4];
-  auto load_w = [&](int gi, uint4 (&dst)[4]) {
-#pragma unroll
-    for (int o = 0; o < 4; ++o) {
-      const int wrow = gi * 16 + c + 4 * o;
-      if (col_ok && 8 * wrow < a.K) dst[o] = ldg_stream_v4(a.qw + (size_t)wrow * N + col0);
-      else dst[o] = make_uint4(0, 0, 0, 0);
+  // lane 0 streams this warp's slice of the CTA's units, kRing ahead; (ib, ig)
+  // is the next unit to copy
+  int ib = first_block, ig = (int)(u0 % a.G), ik = 0;
+  auto issue = [&]() {
+    const int s = ik % kRing;
+    mbar_arrive_expect_tx(&bar[s], kTileBytes);
+    tma_load_2d(ring + s * kTileBytes, &tmW, &bar[s], ib * kGemvCols + warp * 32, ig * 16);
+    ++ik;
+    if (++ig == a.G) {
+      ig = 0;
+      ++ib;
     }
   };
-  if (g_begin < g_end) load_w(g_begin, wq);
+  if (lane == 0) {
+    prefetch_tmap(&tmW);
+    for (int k = 0; k < kRing && k < nu; ++k) issue();
+  }
 
-#pragma unroll 1
-  for (int gi = g_begin; gi < g_end; ++gi) {
-    if (gi + 1 < g_end) load_w(gi + 1, wn);
-    dq.load_group(a, gi, col0, col_ok);
+  float acc[NT][2][4];
+  auto zero_acc = [&]() {
 #pragma unroll
-    for (int o = 0; o < 4; ++o) {
-      const int row0 = gi * 128 + 8 * (c + 4 * o);  // first K row of this lane's word-row
-      // activations of the same 8 rows, for this lane's token(s)
-      uint32_t b[NT][4];
+    for (int t = 0; t < NT; ++t)
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int tok = 8 * t + g;
-        uint4 xv = make_uint4(0, 0, 0, 0);
-        if (tok < a.M && row0 < a.K) xv = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)tok * a.K + row0));
-        b[t][0] = prmt(xv.x, xv.z, 0x5410u);  // rows (0, 4)
-        b[t][1] = prmt(xv.x, xv.z, 0x7632u);  // rows (1, 5)
-        b[t][2] = prmt(xv.y, xv.w, 0x5410u);  // rows (2, 6)
-        b[t][3] = prmt(xv.y, xv.w, 0x7632u);  // rows (3, 7)
-      }
-      uint32_t pr[4][4];
-      dq.word_row(a, wq[o], row0, col0, col_ok, pr);
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[t][r][i] = 0.f;
+  };
+  zero_acc();
+
+  // The warp's slice of column block b is finished: write it directly when
+  // this CTA owns the whole block, else through a partial and a ticket.
+  auto flush = [&](int b) {
+    const int col0 = b * kGemvCols + warp * 32 + 4 * gl;
+    const bool ok = col0 < a.N;
+    const int i_first = R.owner((long long)b * a.G);
+    const int i_last = R.owner((long long)(b + 1) * a.G - 1);
+    if (i_first == i_last) {
+      if (!ok) return;
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int tok = 8 * t + 2 * c;
+          const int col = col0 + 2 * r;
+          if (tok < a.M)
+            *reinterpret_cast<uint32_t*>(a.Y + (size_t)tok * a.N + col) =
+                pack2_rn(acc[t][r][0], acc[t][r][2], BF16);
+          if (tok + 1 < a.M)
+            *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * a.N + col) =
+                pack2_rn(acc[t][r][1], acc[t][r][3], BF16);
+        }
+      return;
+    }
+    const int seg = (b == first_block) ? 0 : 1;
+    float* slot = a.partial + ((size_t)(cta * 2 + seg) * kWarps + warp) * a.M * 32;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const uint32_t a0[4] = {pr[2 * r][0], pr[2 * r + 1][0], pr[2 * r][1], pr[2 * r + 1][1]};
-        const uint32_t a1[4] = {pr[2 * r][2], pr[2 * r + 1][2], pr[2 * r][3], pr[2 * r + 1][3]};
+        const int tok = 8 * t + 2 * c;
+        const int cl = 4 * gl + 2 * r;
+        if (tok < a.M) *reinterpret_cast<float2*>(slot + tok * 32 + cl) = make_float2(acc[t][r][0], acc[t][r][2]);
+        if (tok + 1 < a.M)
+          *reinterpret_cast<float2*>(slot + (tok + 1) * 32 + cl) = make_float2(acc[t][r][1], acc[t][r][3]);
+      }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    int* ticket = a.counters + b * kWarps + warp;
+    if (lane == 0) {
+      last = atomicAdd(ticket, 1) == i_last - i_first;
+      if (last) {
+        *ticket = 0;  // ready for the next call
+        __threadfence();
+      }
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (!last) return;
+    const int col = b * kGemvCols + warp * 32 + lane;
+    if (col >= a.N) return;
+    // contributor i wrote this block as its first (slot 0) or last (slot 1)
+    // block; sum in contributor order, loads issued ahead of the adds
+    for (int tok = 0; tok < a.M; ++tok) {
+      float sum = 0.f;
+      for (int i0 = i_first; i0 <= i_last; i0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j;
+          v[j] = 0.f;
+          if (i <= i_last) {
+            const int sg = (b == (int)(R.start(i) / a.G)) ? 0 : 1;
+            v[j] = __ldcg(a.partial + ((size_t)(i * 2 + sg) * kWarps + warp) * a.M * 32 + tok * 32 + lane);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (i0 + j <= i_last) sum += v[j];
+      }
+      a.Y[(size_t)tok * a.N + col] = (uint16_t)(pack2_rn(sum, 0.f, BF16) & 0xFFFFu);
+    }
+  };
+
+  int cur_b = -1;
+  int b = first_block, g = (int)(u0 % a.G);  // current unit
+  if (nu > 0) dq.fetch(a, g, b * kGemvCols + warp * 32, lane);
+#pragma unroll 1
+  for (int k = 0; k < nu; ++k) {
+    if (b != cur_b) {
+      if (cur_b >= 0) {
+        flush(cur_b);
+        zero_acc();
+      }
+      cur_b = b;
+    }
+    const int col0 = b * kGemvCols + warp * 32 + 4 * gl;
+    const bool ok = col0 < a.N;
+    dq.publish(lane);
+    __syncwarp();
+    dq.begin(gl);
+    int bn = b, gn = g + 1;  // next unit
+    if (gn == a.G) {
+      gn = 0;
+      ++bn;
+    }
+    if (k + 1 < nu) dq.fetch(a, gn, bn * kGemvCols + warp * 32, lane);  // its constants, early
+    const int s = k % kRing;
+    if (!mbar_wait(&bar[s], (k / kRing) & 1, &abort_flag, a.dev_status, kWaitLimitNs)) {
+      // let this warp's copies in flight land before its shared memory goes away
+      for (int kk = k; kk < k + kRing && kk < nu; ++kk)
+        (void)mbar_drain(&bar[kk % kRing], (kk / kRing) & 1, kWaitLimitNs);
+      return;
+    }
+    const uint8_t* st = ring + s * kTileBytes;
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      const int r = tile_row(c, o);
+      const uint4 wv = *reinterpret_cast<const uint4*>(st + r * 128 + ((gl ^ (r & 7)) << 4));
+      if (o == 3) {
+        __syncwarp();
+        if (lane == 0 && k + kRing < nu) {
+          fence_proxy_async_smem();  // the warp's reads of this stage precede the next copy into it
+          issue();
+        }
+      }
+      const int row0 = g * 128 + 8 * r;
+      uint32_t bf[NT][4];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int tok = 8 * t + gl;
+        uint4 xv = make_uint4(0, 0, 0, 0);
+        if (tok < a.M && row0 < a.K) xv = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)tok * a.K + row0));
+        bf[t][0] = prmt(xv.x, xv.z, 0x5410u);  // rows (0, 4)
+        bf[t][1] = prmt(xv.x, xv.z, 0x7632u);  // rows (1, 5)
+        bf[t][2] = prmt(xv.y, xv.w, 0x5410u);  // rows (2, 6)
+        bf[t][3] = prmt(xv.y, xv.w, 0x7632u);  // rows (3, 7)
+      }
+      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        uint32_t pa[4], pb[4];
+        dq.word(a, o, ws[2 * rr], 2 * rr, row0, col0, ok, pa);
+        dq.word(a, o, ws[2 * rr + 1], 2 * rr + 1, row0, col0, ok, pb);
+        const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+        const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          mma_16816<BF16>(acc[t][r], a0, b[t][0], b[t][1]);
-          mma_16816<BF16>(acc[t][r], a1, b[t][2], b[t][3]);
+          mma_16816<BF16>(acc[t][rr], a0, bf[t][0], bf[t][1]);
+          mma_16816<BF16>(acc[t][rr], a1, bf[t][2], bf[t][3]);
         }
       }
     }
-#pragma unroll
-    for (int o = 0; o < 4; ++o) wq[o] = wn[o];
+    b = bn;
+    g = gn;
   }
+  if (cur_b >= 0) flush(cur_b);
+}
 
-  // D fragment: acc[t][r] = {(tok 2c, colA), (tok 2c+1, colA), (tok 2c, colB), (tok 2c+1, colB)}
-  // with colA = col0 + 2r, colB = colA + 1, tok relative to 8t.
-  if (a.splits == 1) {
-    if (!col_ok) return;
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int tok = 8 * t + 2 * c;
-        const int col = col0 + 2 * r;
-        if (tok < a.M) *reinterpret_cast<uint32_t*>(a.Y + (size_t)tok * N + col) = pack2_rn(acc[t][r][0], acc[t][r][2], BF16);
-        if (tok + 1 < a.M) *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * N + col) = pack2_rn(acc[t][r][1], acc[t][r][3], BF16);
-      }
-    return;
-  }
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-  if (col_ok) {
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int tok = 8 * t + 2 * c;
-        const int col = col0 + 2 * r;
-        if (tok < a.M)
-          *reinterpret_cast<float2*>(a.partial + ((size_t)split * a.M + tok) * N + col) = make_float2(acc[t][r][0], acc[t][r][2]);
-        if (tok + 1 < a.M)
-          *reinterpret_cast<float2*>(a.partial + ((size_t)split * a.M + tok + 1) * N + col) = make_float2(acc[t][r][1], acc[t][r][3]);
-      }
+PFN_encodeTiled encode_fn() {
+  static PFN_encodeTiled fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled>(ptr);
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(a.counters + blockIdx.x, 1);
-    s_last = (prev == a.splits - 1);
-    if (s_last) {
-      a.counters[blockIdx.x] = 0;  // ready for the next call
-      __threadfence();
-    }
+  return fn;
+}
+
+template <int NT, int FMT, bool BF16>
+cudaError_t launch_one(const CUtensorMap& tm, const GemvArgs& a, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         gemv_smem(ring_depth<NT>()));
+    if (e != cudaSuccess) return e;
+    // as much shared memory as the SM has, so that the intended number of
+    // CTAs fits next to each other
+    e = cudaFuncSetAttribute(gemv_kernel<NT, FMT, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr = true;
   }
-  __syncthreads();
-  if (!s_last) return;
-  const int col = col_blk + threadIdx.x;
-  if (col >= a.N) return;
-  for (int tok = 0; tok < a.M; ++tok) {
-    float s = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) s += __ldcg(a.partial + ((size_t)sp * a.M + tok) * N + col);
-    const uint32_t v = pack2_rn(s, 0.f, BF16);
-    a.Y[(size_t)tok * N + col] = (uint16_t)(v & 0xFFFFu);
-  }
+  gemv_kernel<NT, FMT, BF16><<<a.ctas, kGemvThreads, gemv_smem(ring_depth<NT>()), st>>>(tm, a);
+  return cudaGetLastError();
 }
 
 template <int FMT>
-static cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st) {
-  dim3 grid(a.N > 0 ? (a.N + kGemvCols - 1) / kGemvCols : 0, a.splits), block(kGemvThreads);
-  if (a.M <= 8) {
-    if (bf16) gemv_kernel<1, FMT, true><<<grid, block, 0, st>>>(a);
-    else gemv_kernel<1, FMT, false><<<grid, block, 0, st>>>(a);
-  } else {
-    if (bf16) gemv_kernel<2, FMT, true><<<grid, block, 0, st>>>(a);
-    else gemv_kernel<2, FMT, false><<<grid, block, 0, st>>>(a);
-  }
-  return cudaGetLastError();
+cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tm;
+  cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)(a.K / 8)};
+  cuuint64_t strides[1] = {(cuuint64_t)a.N * 4};
+  cuuint32_t box[2] = {32, 16};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.qw), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (a.M <= 8) return bf16 ? launch_one<1, FMT, true>(tm, a, st) : launch_one<1, FMT, false>(tm, a, st);
+  return bf16 ? launch_one<2, FMT, true>(tm, a, st) : launch_one<2, FMT, false>(tm, a, st);
 }
+
+}  // namespace
 
 cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st) {
   return a.g_idx ? launch_gemv<kInt4Act>(a, bf16, st) : launch_gemv<kInt4>(a, bf16, st);
 }
 
-cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st) {
-  return launch_gemv<kNF4>(a, bf16, st);
-}
+cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st) { return launch_gemv<kNF4>(a, bf16, st); }
 
-GemvPlan gemv_plan(int M, int N, int K, int rows_per_group) {
+GemvPlan gemv_plan(int M, int N, int K, int fmt) {
   GemvPlan p{};
   p.blocks_n = (N + kGemvCols - 1) / kGemvCols;
-  const int G = (K + 127) / 128;  // chunks of 128 rows
-  (void)rows_per_group;
-  int s = p.blocks_n > 0 ? (kGemvTargetCTAs + p.blocks_n / 2) / p.blocks_n : 1;
-  s = s < 1 ? 1 : (s > G ? G : s);
-  p.groups_per_split = G > 0 ? (G + s - 1) / s : 1;
-  p.splits = G > 0 ? (G + p.groups_per_split - 1) / p.groups_per_split : 1;
-  if (p.splits > 1 && M > 0) {
-    p.workspace_bytes = kCountersBytes + (size_t)p.splits * M * N * sizeof(float);
-  }
+  p.G = (K + 127) / 128;
+  const long long U = (long long)p.blocks_n * p.G;
+  // at least kMinUnits units (64 KB of weights) per CTA: below that the
+  // per-CTA start-up and the split reduction cost more than the bytes
+  constexpr long long kMinUnits = 4;
+  long long target = kNumSMs * gemv_ctas_per_sm(M, fmt);
+  const long long cap = U / kMinUnits > 0 ? U / kMinUnits : 1;
+  if (target > cap) target = cap;
+  p.ctas = (int)target;
+  // sized for the largest grid any format may use, so one size serves all
+  if (M > 0 && N > 0 && K > 0)
+    p.workspace_bytes =
+        kCountersBytes + (size_t)kNumSMs * kGemvMaxCTAsPerSM * 2 * kWarps * (size_t)M * 32 * sizeof(float);
   return p;
 }
 

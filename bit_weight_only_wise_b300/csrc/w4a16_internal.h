@@ -12,29 +12,33 @@ namespace w4a16 {
 constexpr int kNumSMs = 148;
 
 // ----------------------------------------------------------- split-K GEMV
-constexpr int kGemvThreads = 256;               // 8 warps
-constexpr int kGemvCols = 256;                  // columns per CTA (32 per warp)
-constexpr int kGemvTargetCTAs = kNumSMs * 4;    // CTAs to aim for
+constexpr int kGemvThreads = 256;            // 8 warps, one 32-column slice each
+constexpr int kGemvCols = 256;               // columns per unit
+enum GemvFmt { kInt4 = 0, kInt4Act = 1, kNF4 = 2 };
+// persistent grid: CTAs resident per SM, by token tiles (M <= 8: one tile of
+// 8 tokens) and format (register and shared-memory budget of each variant)
+constexpr int kGemvMaxCTAsPerSM = 3;
+constexpr int gemv_ctas_per_sm(int M, int) { return M <= 8 ? 3 : 2; }
 // The workspace starts with a fixed-size area of split-K tickets (one int per
-// column block) and the fp32 partial sums follow it.  The area's size does not
-// depend on the shape, so partial sums of one call never land where a later
-// call with another shape keeps its tickets.
-constexpr int kMaxColBlocks = 4096;
-constexpr size_t kCountersBytes = kMaxColBlocks * sizeof(int);
+// 32-column slice) and the fp32 partial sums follow it.  The area's size does
+// not depend on the shape, so partial sums of one call never land where a
+// later call with another shape keeps its tickets.
+constexpr int kMaxColBlocks = 4096;          // N <= 4096 * 256
+constexpr size_t kCountersBytes = (size_t)kMaxColBlocks * (kGemvCols / 32) * sizeof(int);
 
 struct GemvPlan {
-  int blocks_n;          // CTAs along N
-  int splits;            // CTAs along K
-  int groups_per_split;  // K groups (128 rows) each split covers
+  int blocks_n;  // 256-column blocks
+  int G;         // 128-row K groups
+  int ctas;      // persistent grid size
   size_t workspace_bytes;
 };
 
-GemvPlan gemv_plan(int M, int N, int K, int rows_per_group);
+GemvPlan gemv_plan(int M, int N, int K, int fmt);
 
 struct GemvArgs {
   const uint16_t* X;
   const uint32_t* qw;
-  const uint16_t* scales;  // INT4: fp16 scales; unused for NF4
+  const uint16_t* scales;  // INT4: fp16 scales
   const uint32_t* qz;      // INT4 packed zeros
   const int32_t* g_idx;    // INT4 act-order map or nullptr
   const float* absmax;     // NF4
@@ -42,10 +46,11 @@ struct GemvArgs {
   uint16_t* Y;
   float* partial;
   int* counters;
+  int* dev_status;
   int M, N, K;
-  int G;                 // number of K groups of `rows_per_group` rows
-  int groups_per_split;
-  int splits;
+  int G;         // 128-row K groups
+  int blocks_n;  // 256-column blocks
+  int ctas;
 };
 
 cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st);

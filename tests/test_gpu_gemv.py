@@ -71,11 +71,14 @@ def test_gemv_deterministic_and_workspace_reuse():
     X = activations(16, K, "f16", 0).cuda()
     Y1 = w4.gemv(X, *dev_t[:3])
     Y2 = w4.gemv(X, *dev_t[:3])
-    Y3 = w4.gemv(X[:3].contiguous(), *dev_t[:3])  # different M through the same workspace
+    Y3 = w4.gemv(X[:3].contiguous(), *dev_t[:3])  # another M (and plan) through the same workspace
     Y4 = w4.gemv(X, *dev_t[:3])
     assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
     assert torch.equal(Y1.view(torch.int16), Y4.view(torch.int16))
-    assert torch.equal(Y3.view(torch.int16), Y1[:3].view(torch.int16))
+    # a different M may split K differently: equal to within rounding
+    assert torch.allclose(Y3.float(), Y1[:3].float(), rtol=1e-2, atol=1e-2)
+    Y5 = w4.gemv(X[:3].contiguous(), *dev_t[:3])
+    assert torch.equal(Y3.view(torch.int16), Y5.view(torch.int16))
 
 
 def test_gemm_entry_dispatches_small_m_to_gemv():
