@@ -38,6 +38,7 @@ _sz = ctypes.c_size_t
 _SIGS = {
     "w4a16_gemm": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
     "w4a16_gemv": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
+    "w4a16_gemv_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp],
     "nf4_gemm": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
     "w4a16_dequant": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "nf4_dequant": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],

@@ -143,6 +143,31 @@ w4a16_status w4a16_quantize(const float* W, int K, int N, int group_size, uint32
 w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const float* codebook16,
                           uint32_t* qweight, float* absmax, cudaStream_t stream);
 
+/*
+ * Allocation-free decode: the same product as w4a16_gemv (INT4, 0 <= M <= 16,
+ * same arguments and results) for callers that cannot allocate a workspace --
+ * e.g. code that runs inside someone else's memory pool, or on a path where
+ * cudaMalloc (which may synchronise the device or fail when memory is
+ * fragmented) is not allowed.  The pages have no counterpart; this is a
+ * library convenience.
+ *
+ * The scratch it needs lives in the library: one static device array of
+ * W4A16_NOALLOC_SCRATCH_BYTES per GPU, held from the time the library is
+ * loaded on that GPU until the process exits.  Calls that would need more
+ * scratch than that return W4A16_ERR_UNSUPPORTED (with the current split-K
+ * plan every M <= 16 fits).  The function allocates and frees nothing.
+ *  - The first call on each device looks up the array's address with that
+ *    device current; make that first call before any stream capture.
+ *  - Each call clears the scratch area that must start at zero, on `stream`.
+ *  - All calls share the one array and it keeps the last call's contents:
+ *    calls that may run at the same time on the GPU (different streams with
+ *    no ordering between them) race and must not be issued.
+ */
+#define W4A16_NOALLOC_SCRATCH_BYTES (16u << 20)
+w4a16_status w4a16_gemv_noalloc(const void* X, const uint32_t* qweight, const void* scales,
+                                const uint32_t* qzeros, const int32_t* g_idx, void* Y, int M, int N, int K,
+                                int group_size, w4a16_dtype dtype, int* dev_status, cudaStream_t stream);
+
 /* Bytes of workspace w4a16_gemm / w4a16_gemv / nf4_gemm need for this
  * shape (0 when none is needed).  Pure host function. */
 size_t w4a16_workspace_bytes(int M, int N, int K);
