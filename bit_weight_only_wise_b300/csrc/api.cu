@@ -116,7 +116,7 @@ w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scal
   if (M <= W4A16_GEMV_MAX_M)
     return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
                           dev_status, stream);
-  if (g_idx) return W4A16_ERR_UNSUPPORTED;
+  if (g_idx && !gemm_act_order_fits(K)) return W4A16_ERR_UNSUPPORTED;
   GemmArgs a{};
   a.X = X;
   a.qw = qweight;

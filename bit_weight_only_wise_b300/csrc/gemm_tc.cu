@@ -49,7 +49,6 @@ constexpr int kStages = 4;
 constexpr int kABufs = 4;
 constexpr int kDqWarps = 8;
 constexpr int kThreads = 32 * (2 + kDqWarps);
-constexpr int kXStageBytes = kMaxBT * kBK * 2;     // 32 KB
 constexpr int kWStageBytes = (kBK / 8) * kBN * 4;  // 4 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemA = 256;  // first A-buffer column; D uses [0, BT)
@@ -67,9 +66,21 @@ struct __align__(8) Bars {
   float cb[16];
 };
 
-constexpr int kSmemBytes = 1024 /* alignment slack */ + kStages * (kXStageBytes + kWStageBytes) + 1024;
+enum { kFmtInt4 = 0, kFmtInt4Act = 1, kFmtNF4 = 2 };
+
+// Act-order keeps every group's (scale, zero) of the CTA's 128 columns in
+// shared memory, so its token tile is capped at 128 to leave room.
+template <int FMT>
+constexpr int max_bt() { return FMT == kFmtInt4Act ? 128 : kMaxBT; }
+template <int FMT>
+constexpr int x_stage_bytes() { return max_bt<FMT>() * kBK * 2; }
+template <int FMT>
+constexpr int smem_fixed() { return 1024 /* alignment slack */ + kStages * (x_stage_bytes<FMT>() + kWStageBytes) + 1024; }
+constexpr int kActTableRowBytes = kBN * 4;  // one group: 128 columns x (scale | zero << 16)
+constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmParams {
+  const int32_t* g_idx;
   const uint16_t* scales;
   const uint32_t* qz;
   const float* absmax;
@@ -81,17 +92,18 @@ struct GemmParams {
   uint32_t idesc;
 };
 
-enum { kFmtInt4 = 0, kFmtNF4 = 2 };
-
 template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sx = smem;                                   // kStages x 32 KB
+  constexpr int kXStageBytes = x_stage_bytes<FMT>();
+  uint8_t* sx = smem;                                                          // kStages X tiles
   uint32_t* sw = reinterpret_cast<uint32_t*>(smem + kStages * kXStageBytes);  // kStages x 4 KB
   Bars* bars = reinterpret_cast<Bars*>(smem + kStages * (kXStageBytes + kWStageBytes));
+  // act-order: [G][128] words, (scale bits | zero << 16), after the barriers
+  uint32_t* act_tab = reinterpret_cast<uint32_t*>(smem + kStages * (kXStageBytes + kWStageBytes) + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -116,6 +128,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmW);
   }
   if (FMT == kFmtNF4 && threadIdx.x < 16) bars->cb[threadIdx.x] = p.codebook[threadIdx.x];
+  if (FMT == kFmtInt4Act) {
+    const int G = p.K / 128;
+    for (int i = threadIdx.x; i < G * kBN; i += kThreads) {
+      const int g = i / kBN, c = i % kBN, n = n0 + c;
+      uint32_t v = 0;
+      if (n < p.N) {
+        const uint32_t sb = p.scales[(size_t)g * p.N + n];
+        const uint32_t z = (p.qz[(size_t)g * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu;
+        v = sb | (z << 16);
+      }
+      act_tab[i] = v;
+    }
+  }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -177,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_raw = 0, z_raw = 0, s_nxt = 0, z_nxt = 0;
     float am = 0.f, am_nxt = 0.f;
     auto fetch = [&](int kb, uint32_t& s_out, uint32_t& z_out, float& am_out) {
-      if (!ok || kb >= nkb) return;
+      if (!ok || kb >= nkb || FMT == kFmtInt4Act) return;
       if (FMT == kFmtInt4) {
         const int grp = kb >> 1;  // 128-row groups, 64-row stages
         s_out = p.scales[(size_t)grp * p.N + n];
@@ -187,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     fetch(0, s_raw, z_raw, am);
-    fetch(FMT == kFmtInt4 ? 2 : 1, s_nxt, z_nxt, am_nxt);
+    fetch(FMT == kFmtNF4 ? 1 : 2, s_nxt, z_nxt, am_nxt);
     uint32_t zmix = dq_zmix_f16(z_raw), s2 = s_raw * 0x10001u;
     DqConstBF16 cbf = dq_const_bf16(z_raw, s_raw);
 
@@ -199,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_raw = s_nxt;
         z_raw = z_nxt;
         am = am_nxt;
-        fetch(FMT == kFmtInt4 ? it + 2 : it + 1, s_nxt, z_nxt, am_nxt);
+        fetch(FMT == kFmtNF4 ? it + 1 : it + 2, s_nxt, z_nxt, am_nxt);
         if (FMT == kFmtInt4) {
           if (BF16) cbf = dq_const_bf16(z_raw, s_raw);
           else {
@@ -219,12 +244,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->empty[s]);
       uint32_t regs[16];
+      if constexpr (FMT == kFmtInt4Act) {
+        // every K row has its own group: rows 64*it + 8*(4h + i) + 2j, +1
+        const int4* gp = reinterpret_cast<const int4*>(p.g_idx + it * kBK + 32 * h);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t* o = regs + 4 * i;
-        if (FMT == kFmtNF4) dq_word_nat_nf4<BF16>(wv[i], bars->cb, am, o);
-        else if (BF16) dq_word_nat_bf16(wv[i], cbf, o);
-        else dq_word_nat_f16(wv[i], zmix, s2, o);
+        for (int i = 0; i < 4; ++i) {
+          const int4 ga = __ldg(gp + 2 * i), gb = __ldg(gp + 2 * i + 1);
+          const int gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t t0 = act_tab[gr[2 * j] * kBN + nl], t1 = act_tab[gr[2 * j + 1] * kBN + nl];
+            const uint32_t z0 = t0 >> 16, z1 = t1 >> 16, s0 = t0 & 0xFFFFu, s1 = t1 & 0xFFFFu;
+            const uint32_t w = wv[i];
+            if (BF16) {
+              const uint32_t sel = (uint32_t)j * 0x0011u + (uint32_t)(4 + j) * 0x1100u;
+              const uint32_t u = prmt(w, w >> 4, sel);
+              regs[4 * i + j] = dq_pair_bf16(lop3_and_or(u, 0x000F000Fu, 0x43004300u), dq_const_bf16_2(z0, s0, z1, s1));
+            } else {
+              const uint32_t u = prmt(w, 0u, 0x1111u * j);
+              const uint32_t zm = (0x6400u | z0) | ((0x5400u | (z1 << 4)) << 16);
+              regs[4 * i + j] = hmul2_f16(hsub2_f16(lop3_and_or(u, 0x00F0000Fu, 0x54006400u), zm), s0 | (s1 << 16));
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t* o = regs + 4 * i;
+          if (FMT == kFmtNF4) dq_word_nat_nf4<BF16>(wv[i], bars->cb, am, o);
+          else if (BF16) dq_word_nat_bf16(wv[i], cbf, o);
+          else dq_word_nat_f16(wv[i], zmix, s2, o);
+        }
       }
       if (!mbar_wait(&bars->a_empty[b], ((it / kABufs) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) {
         alive = false;
@@ -307,23 +357,32 @@ cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const Gemm
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+                                         kMaxSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_tc_kernel<FMT, BF16><<<grid, kThreads, kSmemBytes, st>>>(tmX, tmW, p);
+  const int smem = smem_fixed<FMT>() + (FMT == kFmtInt4Act ? (p.K / 128) * kActTableRowBytes : 0);
+  if (smem > kMaxSmem) return cudaErrorInvalidValue;
+  gemm_tc_kernel<FMT, BF16><<<grid, kThreads, smem, st>>>(tmX, tmW, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int gemm_tokens_per_cta(int M) {
-  if (M >= kMaxBT) return kMaxBT;
+int gemm_tokens_per_cta(int M, bool act_order) {
+  const int cap = act_order ? max_bt<kFmtInt4Act>() : kMaxBT;
+  if (M >= cap) return cap;
   return (M + 31) / 32 * 32;
 }
 
+bool gemm_act_order_fits(int K) {
+  return smem_fixed<kFmtInt4Act>() + (K / 128) * kActTableRowBytes <= kMaxSmem;
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st) {
-  const int BT = gemm_tokens_per_cta(a.M);
+  const bool act = a.g_idx != nullptr;
+  if (act && (nf4 || !gemm_act_order_fits(a.K))) return cudaErrorInvalidValue;
+  const int BT = gemm_tokens_per_cta(a.M, act);
   CUtensorMap tmX, tmW;
   const CUtensorMapDataType xdt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (!encode_2d(&tmX, xdt, a.X, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, kBK, (uint32_t)BT,
@@ -333,6 +392,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
                  kBN, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   GemmParams p{};
+  p.g_idx = a.g_idx;
   p.scales = a.scales;
   p.qz = a.qz;
   p.absmax = a.absmax;
@@ -346,6 +406,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   p.idesc = sm100::idesc_f16(bf16, kBN, BT);
   dim3 grid((a.N + kBN - 1) / kBN, (a.M + BT - 1) / BT);
   if (nf4) return bf16 ? launch_tc<kFmtNF4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtNF4, false>(tmX, tmW, p, grid, st);
+  if (act)
+    return bf16 ? launch_tc<kFmtInt4Act, true>(tmX, tmW, p, grid, st)
+                : launch_tc<kFmtInt4Act, false>(tmX, tmW, p, grid, st);
   return bf16 ? launch_tc<kFmtInt4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtInt4, false>(tmX, tmW, p, grid, st);
 }
 

@@ -71,7 +71,9 @@ struct GemmArgs {
 };
 
 // Tokens per CTA (the MMA's N) the tensor-core kernel uses for M tokens.
-int gemm_tokens_per_cta(int M);
+int gemm_tokens_per_cta(int M, bool act_order);
+// Whether the act-order variant's per-CTA (scale, zero) table fits for this K.
+bool gemm_act_order_fits(int K);
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st);
 
 // ------------------------------------------------------- standalone kernels

@@ -125,3 +125,50 @@ def test_nf4_gemm_full_size_sampled():
         rows = _sample_rows(M)
         Y_ref, A = nf4_expected(W, X.double().numpy()[rows], cb, "bf16", cols)
         assert_close(to_f64(Y)[np.ix_(rows, cols)], Y_ref, A, f"nf4 full M={M}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,K,N", [(17, 512, 264), (64, 1024, 384), (200, 2048, 136)])
+def test_gemm_act_order_small(dtype, M, K, N):
+    from synth import act_order_g_idx
+
+    W = student_t_weights(K, N, 5, 0.01, M)
+    g_idx = act_order_g_idx(K, 128, M)
+    dev_t, _ = _int4_dev(W, g_idx)
+    X = activations(M, K, dtype, M)
+    Y = w4.gemm(X.cuda(), *dev_t[:3], g_idx=dev_t[3])
+    Y_ref, A = int4_expected(W, X.double().numpy(), dtype, None, g_idx)
+    assert_close(to_f64(Y), Y_ref, A, f"act-order gemm M={M} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_gemm_act_order_one_hot_exact(dtype):
+    from synth import act_order_g_idx
+
+    K, N = 1024, 264
+    W = gaussian_weights(K, N, 0.02, 4)
+    g_idx = act_order_g_idx(K, 128, 4)
+    dev_t, (q, sc, z) = _int4_dev(W, g_idx)
+    rows = np.arange(0, K, 13)[:48]
+    X = torch.zeros((rows.size, K), dtype=TDT[dtype])
+    X[torch.arange(rows.size), torch.from_numpy(rows)] = 1.0
+    Y = w4.gemm(X.cuda(), *dev_t[:3], g_idx=dev_t[3])
+    assert np.array_equal(bits(Y), int4.dequant(q, sc, z, dtype, 128, g_idx)[rows])
+
+
+@pytest.mark.parametrize("K,N", WORKLOADS["act_order"].shapes)
+def test_gemm_act_order_full_size_m64(K, N):
+    from synth import act_order_g_idx
+
+    wl = WORKLOADS["act_order"]
+    W = weights_for(wl, K, N, 0)
+    g_idx = act_order_g_idx(K, 128, 0)
+    (qw, sc, qz, gi), _ = _int4_dev(W, g_idx)
+    cols = sample_columns(N)
+    X = activations(64, K, wl.dtype, 64)
+    st = _status()
+    Y = w4.gemm(X.cuda(), qw, sc, qz, g_idx=gi, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    Y_ref, A = int4_expected(W, X.double().numpy(), wl.dtype, cols, g_idx)
+    assert_close(to_f64(Y)[:, cols], Y_ref, A, f"act-order {K}x{N} M=64")
