@@ -47,12 +47,18 @@ namespace {
 
 constexpr int kWarps = kGemvThreads / 32;  // 8 column slices per CTA
 constexpr int kTileBytes = 16 * 32 * 4;    // 16 word-rows x 32 columns
+// the unit's activations ride in the same stage: 8 tokens per tile x 128 rows
+template <int NT>
+constexpr int x_tile_bytes() { return NT * 8 * 128 * 2; }
+template <int NT>
+constexpr int stage_bytes() { return kTileBytes + x_tile_bytes<NT>(); }
 // TMA stages per warp.  Measured on B300: streaming 2-KB boxes runs at ~82%
 // of the copy bandwidth with about 48 copies outstanding per SM (3 CTAs x 8
 // warps x 2, or 2 x 8 x 3); twice as many outstanding copies halve the rate.
 template <int NT>
-constexpr int ring_depth() { return NT == 1 ? 2 : 3; }
-constexpr int gemv_smem(int ring) { return 1024 + kWarps * ring * kTileBytes; }
+constexpr int ring_depth() { return 2; }
+template <int NT>
+constexpr int gemv_smem() { return 1024 + kWarps * ring_depth<NT>() * stage_bytes<NT>(); }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 template <bool BF16>
@@ -220,8 +226,9 @@ struct Range {
 
 template <int NT, int FMT, bool BF16>
 __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 16, FMT))
-    gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const GemvArgs a) {
   constexpr int kRing = ring_depth<NT>();
+  constexpr int kStage = stage_bytes<NT>();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kWarps][kRing];
   __shared__ float s_cb[16];
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int gl = lane >> 2, c = lane & 3;
-  uint8_t* ring = smem + warp * (kRing * kTileBytes);
+  uint8_t* ring = smem + warp * (kRing * kStage);
   uint64_t* bar = full[warp];
   volatile int abort_flag = 0;  // per-warp pipeline: nobody else raises it
 
@@ -255,23 +262,43 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   }
   __syncwarp();
 
-  // lane 0 streams this warp's slice of the CTA's units, kRing ahead; (ib, ig)
-  // is the next unit to copy
-  int ib = first_block, ig = (int)(u0 % a.G), ik = 0;
-  auto issue = [&]() {
-    const int s = ik % kRing;
-    mbar_arrive_expect_tx(&bar[s], kTileBytes);
-    tma_load_2d(ring + s * kTileBytes, &tmW, &bar[s], ib * kGemvCols + warp * 32, ig * 16);
-    ++ik;
-    if (++ig == a.G) {
-      ig = 0;
-      ++ib;
+  // lane 0 streams this warp's slice of the CTA's units, kRing ahead: (tx, ty)
+  // is the TMA coordinate of the next unit to copy, is_ its stage
+  int tx = first_block * kGemvCols + warp * 32, ty = (int)(u0 % a.G) * 16, is_ = 0;
+  const int ty_end = a.G * 16;
+  auto advance = [&]() {
+    is_ = (is_ + 1 == kRing) ? 0 : is_ + 1;
+    ty += 16;
+    if (ty == ty_end) {
+      ty = 0;
+      tx += kGemvCols;
     }
   };
+  auto issue = [&]() {
+    mbar_arrive_expect_tx(&bar[is_], kStage);
+    tma_load_2d(ring + is_ * kStage, &tmW, &bar[is_], tx, ty);
+    tma_load_2d(ring + is_ * kStage + kTileBytes, &tmX, &bar[is_], ty * 8, 0);
+    advance();
+  };
+  // The packed weights do not depend on the previous kernel in the stream, so
+  // the first stages' weight copies start before waiting for it; activations
+  // and the workspace are touched only after griddep_wait.
+  int first_ty[kRing];
+  const int n_first = nu < kRing ? nu : kRing;
   if (lane == 0) {
     prefetch_tmap(&tmW);
-    for (int k = 0; k < kRing && k < nu; ++k) issue();
+    prefetch_tmap(&tmX);
+    for (int k = 0; k < n_first; ++k) {
+      first_ty[k] = ty;
+      mbar_arrive_expect_tx(&bar[is_], kStage);
+      tma_load_2d(ring + is_ * kStage, &tmW, &bar[is_], tx, ty);
+      advance();
+    }
   }
+  griddep_wait();
+  if (lane == 0)
+    for (int k = 0; k < n_first; ++k) tma_load_2d(ring + k * kStage + kTileBytes, &tmX, &bar[k], first_ty[k] * 8, 0);
+  griddep_launch_dependents();
 
   float acc[NT][2][4];
   auto zero_acc = [&]() {
@@ -336,30 +363,43 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
     const int col = b * kGemvCols + warp * 32 + lane;
     if (col >= a.N) return;
     // contributor i wrote this block as its first (slot 0) or last (slot 1)
-    // block; sum in contributor order, loads issued ahead of the adds
-    for (int tok = 0; tok < a.M; ++tok) {
-      float sum = 0.f;
-      for (int i0 = i_first; i0 <= i_last; i0 += 8) {
-        float v[8];
+    // block; sum in contributor order (deterministic), all tokens of a
+    // contributor loaded at once and two contributors in flight
+    float sum[8 * NT];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + j;
-          v[j] = 0.f;
-          if (i <= i_last) {
-            const int sg = (b == (int)(R.start(i) / a.G)) ? 0 : 1;
-            v[j] = __ldcg(a.partial + ((size_t)(i * 2 + sg) * kWarps + warp) * a.M * 32 + tok * 32 + lane);
-          }
-        }
+    for (int t = 0; t < 8 * NT; ++t) sum[t] = 0.f;
+#pragma unroll 2
+    for (int i = i_first; i <= i_last; ++i) {
+      const int sg = (b == (int)(R.start(i) / a.G)) ? 0 : 1;
+      const float* pp = a.partial + ((size_t)(i * 2 + sg) * kWarps + warp) * a.M * 32 + lane;
+      float v[8 * NT];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (i0 + j <= i_last) sum += v[j];
-      }
-      a.Y[(size_t)tok * a.N + col] = (uint16_t)(pack2_rn(sum, 0.f, BF16) & 0xFFFFu);
+      for (int t = 0; t < 8 * NT; ++t) v[t] = t < a.M ? __ldcg(pp + t * 32) : 0.f;
+#pragma unroll
+      for (int t = 0; t < 8 * NT; ++t) sum[t] += v[t];
     }
+#pragma unroll
+    for (int t = 0; t < 8 * NT; ++t)
+      if (t < a.M) a.Y[(size_t)t * a.N + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
   };
+
+  // lane-invariant parts of the shared-memory and activation addresses
+  uint32_t lds_off[4];
+  int xrow[4];
+#pragma unroll
+  for (int o = 0; o < 4; ++o) {
+    const int r = tile_row(c, o);
+    lds_off[o] = (uint32_t)(r * 128 + ((gl ^ (r & 7)) << 4));
+    xrow[o] = 8 * r;
+  }
+  // this lane's activations in a stage: token 8t + gl, rows 8r .. 8r + 7
+  const uint32_t x_lane = (uint32_t)(kTileBytes + gl * 256);
+  const uint32_t ring_s = smem_u32(ring);
 
   int cur_b = -1;
   int b = first_block, g = (int)(u0 % a.G);  // current unit
+  int s = 0;
+  uint32_t phase = 0;
   if (nu > 0) dq.fetch(a, g, b * kGemvCols + warp * 32, lane);
 #pragma unroll 1
   for (int k = 0; k < nu; ++k) {
@@ -381,32 +421,45 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
       ++bn;
     }
     if (k + 1 < nu) dq.fetch(a, gn, bn * kGemvCols + warp * 32, lane);  // its constants, early
-    const int s = k % kRing;
-    if (!mbar_wait(&bar[s], (k / kRing) & 1, &abort_flag, a.dev_status, kWaitLimitNs)) {
+    if (!mbar_wait(&bar[s], phase, &abort_flag, a.dev_status, kWaitLimitNs)) {
       // let this warp's copies in flight land before its shared memory goes away
-      for (int kk = k; kk < k + kRing && kk < nu; ++kk)
-        (void)mbar_drain(&bar[kk % kRing], (kk / kRing) & 1, kWaitLimitNs);
-      return;
-    }
-    const uint8_t* st = ring + s * kTileBytes;
-#pragma unroll
-    for (int o = 0; o < 4; ++o) {
-      const int r = tile_row(c, o);
-      const uint4 wv = *reinterpret_cast<const uint4*>(st + r * 128 + ((gl ^ (r & 7)) << 4));
-      if (o == 3) {
-        __syncwarp();
-        if (lane == 0 && k + kRing < nu) {
-          fence_proxy_async_smem();  // the warp's reads of this stage precede the next copy into it
-          issue();
+      for (int kk = k, ss = s, ph = phase; kk < k + kRing && kk < nu; ++kk) {
+        (void)mbar_drain(&bar[ss], ph, kWaitLimitNs);
+        if (++ss == kRing) {
+          ss = 0;
+          ph ^= 1;
         }
       }
-      const int row0 = g * 128 + 8 * r;
+      return;
+    }
+    const uint32_t st = ring_s + (uint32_t)(s * kStage);
+    // read the whole stage first and hand it back to the TMA right away, so
+    // the next copy overlaps this unit's arithmetic
+    uint4 wvs[4], xvs[NT][4];
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(wvs[o].x), "=r"(wvs[o].y), "=r"(wvs[o].z), "=r"(wvs[o].w)
+                   : "r"(st + lds_off[o]));
+#pragma unroll
+      for (int t = 0; t < NT; ++t)  // zero beyond M and K: the copy fills out-of-range elements with 0
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(xvs[t][o].x), "=r"(xvs[t][o].y), "=r"(xvs[t][o].z), "=r"(xvs[t][o].w)
+                     : "r"(st + x_lane + (uint32_t)(t * 8 * 256 + 2 * xrow[o])));
+    }
+    __syncwarp();
+    if (lane == 0 && k + kRing < nu) {
+      fence_proxy_async_smem();  // the warp's reads of this stage precede the next copy into it
+      issue();
+    }
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      const uint4 wv = wvs[o];
+      const int row0 = g * 128 + xrow[o];
       uint32_t bf[NT][4];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const int tok = 8 * t + gl;
-        uint4 xv = make_uint4(0, 0, 0, 0);
-        if (tok < a.M && row0 < a.K) xv = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)tok * a.K + row0));
+        const uint4 xv = xvs[t][o];
         bf[t][0] = prmt(xv.x, xv.z, 0x5410u);  // rows (0, 4)
         bf[t][1] = prmt(xv.x, xv.z, 0x7632u);  // rows (1, 5)
         bf[t][2] = prmt(xv.y, xv.w, 0x5410u);  // rows (2, 6)
@@ -426,6 +479,10 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
           mma_16816<BF16>(acc[t][rr], a1, bf[t][2], bf[t][3]);
         }
       }
+    }
+    if (++s == kRing) {
+      s = 0;
+      phase ^= 1;
     }
     b = bn;
     g = gn;
@@ -452,10 +509,20 @@ PFN_encodeTiled encode_fn() {
 
 template <int NT, int FMT, bool BF16>
 cudaError_t launch_one(const CUtensorMap& tm, const GemvArgs& a, cudaStream_t st) {
+  auto enc = encode_fn();
+  CUtensorMap tx;  // X [M, K], boxes of 128 rows x 8*NT tokens
+  cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+  cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+  cuuint32_t box[2] = {128, (cuuint32_t)(8 * NT)};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(a.X), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gemv_smem(ring_depth<NT>()));
+                                         gemv_smem<NT>());
     if (e != cudaSuccess) return e;
     // as much shared memory as the SM has, so that the intended number of
     // CTAs fits next to each other
@@ -464,8 +531,19 @@ cudaError_t launch_one(const CUtensorMap& tm, const GemvArgs& a, cudaStream_t st
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  gemv_kernel<NT, FMT, BF16><<<a.ctas, kGemvThreads, gemv_smem(ring_depth<NT>()), st>>>(tm, a);
-  return cudaGetLastError();
+  // programmatic dependent launch: this grid may start while the previous
+  // kernel on the stream finishes (it waits for it before touching its data)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.ctas);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = gemv_smem<NT>();
+  cfg.stream = st;
+  cudaLaunchAttribute attr_pdl[1];
+  attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr_pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<NT, FMT, BF16>, tm, tx, a);
 }
 
 template <int FMT>
