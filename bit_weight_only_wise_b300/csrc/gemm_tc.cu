@@ -47,7 +47,12 @@ constexpr int kBK = 64;        // K rows per stage
 constexpr int kMaxBT = 256;    // tokens per CTA (MMA N)
 constexpr int kStages = 4;
 constexpr int kABufs = 4;
-constexpr int kDqWarps = 8;
+#ifndef W4A16_GEMM_DQ_WARPS
+#define W4A16_GEMM_DQ_WARPS 16
+#endif
+constexpr int kDqWarps = W4A16_GEMM_DQ_WARPS;     // 8 or 16 dequantizing warps
+constexpr int kParts = kDqWarps / 4;              // warps sharing one TMEM lane quarter
+constexpr int kWords = (kBK / 8) / kParts;        // packed words per thread per stage
 constexpr int kThreads = 32 * (2 + kDqWarps);
 constexpr int kWStageBytes = (kBK / 8) * kBN * 4;  // 4 KB
 constexpr uint32_t kTmemCols = 512;
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- dequant + epilogue
     const int dw = warp - 2;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-    const int h = dw >> 2;         // which 4 word-rows of a stage
+    const int h = dw >> 2;         // which kWords word-rows of a stage
     const int nl = quarter * 32 + lane;
     const int n = n0 + nl;
     const bool ok = n < p.N;
@@ -237,18 +242,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         alive = false;
         break;
       }
-      uint32_t wv[4];
+      uint32_t wv[kWords];
       const uint32_t* wst = sw + s * (kWStageBytes / 4);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) wv[i] = wst[(4 * h + i) * kBN + nl];
+      for (int i = 0; i < kWords; ++i) wv[i] = wst[(kWords * h + i) * kBN + nl];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->empty[s]);
-      uint32_t regs[16];
+      uint32_t regs[4 * kWords];
       if constexpr (FMT == kFmtInt4Act) {
-        // every K row has its own group: rows 64*it + 8*(4h + i) + 2j, +1
-        const int4* gp = reinterpret_cast<const int4*>(p.g_idx + it * kBK + 32 * h);
+        // every K row has its own group: rows 64*it + 8*(kWords*h + i) + 2j, +1
+        const int4* gp = reinterpret_cast<const int4*>(p.g_idx + it * kBK + 8 * kWords * h);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kWords; ++i) {
           const int4 ga = __ldg(gp + 2 * i), gb = __ldg(gp + 2 * i + 1);
           const int gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kWords; ++i) {
           uint32_t* o = regs + 4 * i;
           if (FMT == kFmtNF4) dq_word_nat_nf4<BF16>(wv[i], bars->cb, am, o);
           else if (BF16) dq_word_nat_bf16(wv[i], cbf, o);
@@ -280,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         alive = false;
         break;
       }
-      tmem_st_x16(tmem + lane_off + kTmemA + 32u * b + 16u * h, regs);
+      if constexpr (kWords == 4) tmem_st_x16(tmem + lane_off + kTmemA + 32u * b + 16u * h, regs);
+      else tmem_st_x8(tmem + lane_off + kTmemA + 32u * b + 8u * h, regs);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -294,14 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool done = mbar_drain(&bars->d_full, 0, kDrainLimitNs);
     tc_fence_after();
     if (done && !*abort) {
-      const int half = p.BT >> 1;
-      for (int c = h * half; c < (h + 1) * half; c += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(tmem + lane_off + (uint32_t)c, v);
+      const int part = p.BT / kParts;  // tokens per warp, a multiple of 8
+      for (int c = h * part; c < (h + 1) * part; c += 8) {
+        uint32_t v[8];
+        tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
         tmem_wait_ld();
         if (ok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             const int m = m0 + c + j;
             if (m < p.M) {
               const uint32_t y = pack2_rn(__uint_as_float(v[j]), 0.f, BF16);
