@@ -94,6 +94,7 @@ struct GemmParams {
   int* dev_status;
   int M, N, K;
   int BT;
+  int token_fast;
   uint32_t idesc;
 };
 
@@ -112,8 +113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBN;
-  const int m0 = blockIdx.y * p.BT;
+  // Rasterization.  When the packed weights are larger than about half of L2,
+  // token tiles vary fastest: the CTAs that share a weight tile run together
+  // and the weights come from DRAM about once.  Otherwise column tiles vary
+  // fastest and the (then L2-resident) weights are shared across a wave.
+  const int n0 = (p.token_fast ? blockIdx.y : blockIdx.x) * kBN;
+  const int m0 = (p.token_fast ? blockIdx.x : blockIdx.y) * p.BT;
   const int nkb = (p.K + kBK - 1) / kBK;
   volatile int* abort = &bars->abort;
 
@@ -410,7 +415,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   p.K = a.K;
   p.BT = BT;
   p.idesc = sm100::idesc_f16(bf16, kBN, BT);
-  dim3 grid((a.N + kBN - 1) / kBN, (a.M + BT - 1) / BT);
+  const unsigned col_tiles = (a.N + kBN - 1) / kBN, tok_tiles = (a.M + BT - 1) / BT;
+  p.token_fast = (size_t)a.K * a.N / 2 > (size_t)64 << 20;
+  dim3 grid = p.token_fast ? dim3(tok_tiles, col_tiles) : dim3(col_tiles, tok_tiles);
   if (nf4) return bf16 ? launch_tc<kFmtNF4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtNF4, false>(tmX, tmW, p, grid, st);
   if (act)
     return bf16 ? launch_tc<kFmtInt4Act, true>(tmX, tmW, p, grid, st)
