@@ -35,7 +35,9 @@
 #include <cuda.h>
 
 #include "dq_common.cuh"
+#include "gemv_common.cuh"
 #include "sm100.cuh"
+#include "tma_host.h"
 #include "w4a16_internal.h"
 
 namespace w4a16 {
@@ -61,28 +63,9 @@ template <int NT>
 constexpr int gemv_smem() { return 1024 + kWarps * ring_depth<NT>() * stage_bytes<NT>(); }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-template <bool BF16>
-__device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-  if (BF16)
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  else
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-
-// The word-row of the 16-row tile that lane quarter-index c reads at step o.
-__device__ __forceinline__ int tile_row(int c, int o) { return 2 * c + 8 * (o & 1) + (o >> 1); }
 
 // ------------------------------------------------------------- dequantizers
 // fetch(): raw constants of a unit, one unit ahead; begin(): turn them into
@@ -215,15 +198,6 @@ struct Dq<kNF4, BF16> {
   }
 };
 
-// ------------------------------------------------------------ stream-K plan
-struct Range {
-  long long U;  // units
-  int P;        // CTAs
-  __device__ __forceinline__ long long start(int i) const { return U * i / P; }
-  // the CTA whose range holds unit u: the largest i with start(i) <= u
-  __device__ __forceinline__ int owner(long long u) const { return (int)(((u + 1) * P - 1) / U); }
-};
-
 template <int NT, int FMT, bool BF16>
 __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 16, FMT))
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const GemvArgs a) {
@@ -311,77 +285,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   };
   zero_acc();
 
-  // The warp's slice of column block b is finished: write it directly when
-  // this CTA owns the whole block, else through a partial and a ticket.
-  auto flush = [&](int b) {
-    const int col0 = b * kGemvCols + warp * 32 + 4 * gl;
-    const bool ok = col0 < a.N;
-    const int i_first = R.owner((long long)b * a.G);
-    const int i_last = R.owner((long long)(b + 1) * a.G - 1);
-    if (i_first == i_last) {
-      if (!ok) return;
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int tok = 8 * t + 2 * c;
-          const int col = col0 + 2 * r;
-          if (tok < a.M)
-            *reinterpret_cast<uint32_t*>(a.Y + (size_t)tok * a.N + col) =
-                pack2_rn(acc[t][r][0], acc[t][r][2], BF16);
-          if (tok + 1 < a.M)
-            *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * a.N + col) =
-                pack2_rn(acc[t][r][1], acc[t][r][3], BF16);
-        }
-      return;
-    }
-    const int seg = (b == first_block) ? 0 : 1;
-    float* slot = a.partial + ((size_t)(cta * 2 + seg) * kWarps + warp) * a.M * 32;
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int tok = 8 * t + 2 * c;
-        const int cl = 4 * gl + 2 * r;
-        if (tok < a.M) *reinterpret_cast<float2*>(slot + tok * 32 + cl) = make_float2(acc[t][r][0], acc[t][r][2]);
-        if (tok + 1 < a.M)
-          *reinterpret_cast<float2*>(slot + (tok + 1) * 32 + cl) = make_float2(acc[t][r][1], acc[t][r][3]);
-      }
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    int* ticket = a.counters + b * kWarps + warp;
-    if (lane == 0) {
-      last = atomicAdd(ticket, 1) == i_last - i_first;
-      if (last) {
-        *ticket = 0;  // ready for the next call
-        __threadfence();
-      }
-    }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (!last) return;
-    const int col = b * kGemvCols + warp * 32 + lane;
-    if (col >= a.N) return;
-    // contributor i wrote this block as its first (slot 0) or last (slot 1)
-    // block; sum in contributor order (deterministic), all tokens of a
-    // contributor loaded at once and two contributors in flight
-    float sum[8 * NT];
-#pragma unroll
-    for (int t = 0; t < 8 * NT; ++t) sum[t] = 0.f;
-#pragma unroll 2
-    for (int i = i_first; i <= i_last; ++i) {
-      const int sg = (b == (int)(R.start(i) / a.G)) ? 0 : 1;
-      const float* pp = a.partial + ((size_t)(i * 2 + sg) * kWarps + warp) * a.M * 32 + lane;
-      float v[8 * NT];
-#pragma unroll
-      for (int t = 0; t < 8 * NT; ++t) v[t] = t < a.M ? __ldcg(pp + t * 32) : 0.f;
-#pragma unroll
-      for (int t = 0; t < 8 * NT; ++t) sum[t] += v[t];
-    }
-#pragma unroll
-    for (int t = 0; t < 8 * NT; ++t)
-      if (t < a.M) a.Y[(size_t)t * a.N + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
-  };
+  auto flush = [&](int b) { flush_block<NT, BF16>(a, R, cta, first_block, warp, lane, b, acc); };
 
   // lane-invariant parts of the shared-memory and activation addresses
   uint32_t lds_off[4];
@@ -458,13 +362,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
       const int row0 = g * 128 + xrow[o];
       uint32_t bf[NT][4];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const uint4 xv = xvs[t][o];
-        bf[t][0] = prmt(xv.x, xv.z, 0x5410u);  // rows (0, 4)
-        bf[t][1] = prmt(xv.x, xv.z, 0x7632u);  // rows (1, 5)
-        bf[t][2] = prmt(xv.y, xv.w, 0x5410u);  // rows (2, 6)
-        bf[t][3] = prmt(xv.y, xv.w, 0x7632u);  // rows (3, 7)
-      }
+      for (int t = 0; t < NT; ++t) x_pairs(xvs[t][o], bf[t]);
       const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
@@ -490,26 +388,9 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   if (cur_b >= 0) flush(cur_b);
 }
 
-typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-PFN_encodeTiled encode_fn() {
-  static PFN_encodeTiled fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_encodeTiled>(ptr);
-  }
-  return fn;
-}
-
 template <int NT, int FMT, bool BF16>
 cudaError_t launch_one(const CUtensorMap& tm, const GemvArgs& a, cudaStream_t st) {
-  auto enc = encode_fn();
+  auto enc = tensor_map_encoder();
   CUtensorMap tx;  // X [M, K], boxes of 128 rows x 8*NT tokens
   cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
   cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
@@ -548,7 +429,7 @@ cudaError_t launch_one(const CUtensorMap& tm, const GemvArgs& a, cudaStream_t st
 
 template <int FMT>
 cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st) {
-  auto enc = encode_fn();
+  auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tm;
   cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)(a.K / 8)};
@@ -566,7 +447,8 @@ cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st) {
-  return a.g_idx ? launch_gemv<kInt4Act>(a, bf16, st) : launch_gemv<kInt4>(a, bf16, st);
+  // plain groups: the warp-specialized kernel (gemv_ws.cu); act-order: this one
+  return a.g_idx ? launch_gemv<kInt4Act>(a, bf16, st) : launch_gemv_ws_int4(a, bf16, st);
 }
 
 cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st) { return launch_gemv<kNF4>(a, bf16, st); }
