@@ -171,18 +171,28 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------- GPU
-def traffic_from_profiles(kernel_src: str):
-    """dram read+write bytes per launch from the committed ncu summary, if it
-    was taken on the current source of the kernel; else None."""
+# the decode kernel's complete source: the ncu traffic figure in profiles/ is
+# used only while these files are unchanged since the capture
+DECODE_SOURCES = ("gemv_ws.cu", "gemv_common.cuh", "dq_common.cuh", "sm100.cuh")
+
+
+def decode_source_sha256() -> str:
     import hashlib
 
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "bit_weight_only_wise_b300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def traffic_from_profiles(kernel: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current source of the kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    src = open(os.path.join(ROOT, "bit_weight_only_wise_b300", "csrc", kernel_src), "rb").read()
-    ent = d.get(kernel_src)
-    if not ent or ent.get("source_sha256") != hashlib.sha256(src).hexdigest():
+    ent = json.load(open(p)).get(kernel)
+    if not ent or ent.get("source_sha256") != decode_source_sha256():
         return None
     return ent
 
@@ -324,7 +334,7 @@ def run_gpu(args):
         v, cores, sample = oracle_sample(args.cpu_seconds)
         cpu = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
 
-    traffic = traffic_from_profiles("gemv.cu")
+    traffic = traffic_from_profiles("gemv_ws_kernel")
     achieved = per_gpu  # algorithmic bytes per launch / mean launch time == stack bytes / step time
     line = {
         "metric": METRIC,
@@ -355,7 +365,7 @@ def run_gpu(args):
             "frac": round(achieved / hbm_peak, 4),
             "peak_source": peak_src,
             "traffic": None if traffic is None else traffic.get("bytes_per_launch"),
-            "kernel": "gemv_kernel (split-K decode)",
+            "kernel": "gemv_ws_kernel (warp-specialized split-K decode)",
             "algorithmic_bytes_per_launch": STACK_BYTES // (LAYERS * 4),
         },
         "prefill": {

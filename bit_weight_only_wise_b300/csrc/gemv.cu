@@ -285,7 +285,10 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   };
   zero_acc();
 
-  auto flush = [&](int b) { flush_block<NT, BF16>(a, R, cta, first_block, warp, lane, b, acc); };
+  int p0 = -1, p1 = -1;  // split blocks whose tickets are still to be taken
+  auto flush = [&](int b) {
+    if (store_block<NT, BF16>(a, R, cta, first_block, warp, lane, b, acc)) (b == first_block ? p0 : p1) = b;
+  };
 
   // lane-invariant parts of the shared-memory and activation addresses
   uint32_t lds_off[4];
@@ -386,6 +389,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
     g = gn;
   }
   if (cur_b >= 0) flush(cur_b);
+  finish_blocks<NT, BF16>(a, R, warp, lane, p0, p1);
 }
 
 template <int NT, int FMT, bool BF16>

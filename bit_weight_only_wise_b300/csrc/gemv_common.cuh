@@ -57,19 +57,21 @@ __device__ __forceinline__ void x_pairs(const uint4& xv, uint32_t bf[4]) {
   bf[3] = prmt(xv.y, xv.w, 0x7632u);
 }
 
-// Warp `warp`'s slice of column block b is finished: write it directly when
-// CTA `cta` owns the whole block, else through a partial and a ticket; the
-// last contributor sums the partials in contributor order (deterministic
-// whatever the arrival order), rounds once and resets the ticket.
+// Warp `warp`'s slice of column block b is finished.  When CTA `cta` owns
+// the whole block the slice is rounded and written to Y here.  Otherwise its
+// fp32 partial goes to the CTA's slot for the block (slot 0 for the CTA's
+// first block, 1 for its last) and the function returns true: the block's
+// ticket is taken later, by finish_blocks, once the CTA has nothing else to
+// do, so that no warp waits on a memory round trip in the middle of its work.
 template <int NT, bool BF16>
-__device__ __forceinline__ void flush_block(const GemvArgs& a, const Range& R, int cta, int first_block, int warp,
+__device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, int cta, int first_block, int warp,
                                             int lane, int b, const float (&acc)[NT][2][4]) {
   const int gl = lane >> 2, c = lane & 3;
   const int col0 = b * kGemvCols + warp * 32 + 4 * gl;
   const int i_first = R.owner((long long)b * a.G);
   const int i_last = R.owner((long long)(b + 1) * a.G - 1);
   if (i_first == i_last) {
-    if (col0 >= a.N) return;
+    if (col0 >= a.N) return false;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -82,7 +84,7 @@ __device__ __forceinline__ void flush_block(const GemvArgs& a, const Range& R, i
           *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * a.N + col) =
               pack2_rn(acc[t][r][1], acc[t][r][3], BF16);
       }
-    return;
+    return false;
   }
   const int seg = (b == first_block) ? 0 : 1;
   float* slot = a.partial + ((size_t)(cta * 2 + seg) * kSliceWarps + warp) * a.M * 32;
@@ -96,25 +98,37 @@ __device__ __forceinline__ void flush_block(const GemvArgs& a, const Range& R, i
       if (tok + 1 < a.M)
         *reinterpret_cast<float2*>(slot + (tok + 1) * 32 + cl) = make_float2(acc[t][r][1], acc[t][r][3]);
     }
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  int* ticket = a.counters + b * kSliceWarps + warp;
-  if (lane == 0) {
-    last = atomicAdd(ticket, 1) == i_last - i_first;
-    if (last) {
-      *ticket = 0;  // ready for the next call
-      __threadfence();
-    }
-  }
-  last = __shfl_sync(0xFFFFFFFFu, last, 0);
-  if (!last) return;
+  return true;
+}
+
+// Sum the partials of split block b for this warp's slice, in contributor
+// order (deterministic whatever order the contributors finished in), round
+// once and write Y.  Contributor i wrote the block as its first block (slot 0)
+// unless its range starts before the block, which only the first contributor's
+// can.  Several contributors' loads are in flight at once.
+template <int NT, bool BF16>
+__device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, int warp, int lane, int b) {
   const int col = b * kGemvCols + warp * 32 + lane;
   if (col >= a.N) return;
-  // contributor i wrote this block as its first (slot 0) or last (slot 1)
-  // block; the partials of kChunk contributors (all tokens) are loaded at
-  // once and added in contributor order, so the sum is deterministic and a
-  // block split over many CTAs costs few round trips
+  const int i_first = R.owner((long long)b * a.G);
+  const int i_last = R.owner((long long)(b + 1) * a.G - 1);
+  const int sg_first = R.start(i_first) == (long long)b * a.G ? 0 : 1;
+  const size_t stride = (size_t)a.M * 32;  // floats per slice slot
+  auto slot = [&](int i) -> const float* {
+    return a.partial + ((size_t)(i * 2 + (i == i_first ? sg_first : 0)) * kSliceWarps + warp) * stride + lane;
+  };
+  if (a.M == 1) {  // single token: sixteen contributors per round trip
+    float sum = 0.f;
+    for (int i0 = i_first; i0 <= i_last; i0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = i0 + j <= i_last ? __ldcg(slot(i0 + j)) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sum += v[j];
+    }
+    a.Y[col] = (uint16_t)(pack2_rn(sum, 0.f, BF16) & 0xFFFFu);
+    return;
+  }
   constexpr int kChunk = NT == 1 ? 4 : 2;
   float sum[8 * NT];
 #pragma unroll
@@ -124,8 +138,7 @@ __device__ __forceinline__ void flush_block(const GemvArgs& a, const Range& R, i
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
       const int i = i0 + j;
-      const int sg = (i <= i_last && b == (int)(R.start(i) / a.G)) ? 0 : 1;
-      const float* pp = a.partial + ((size_t)(i * 2 + sg) * kSliceWarps + warp) * a.M * 32 + lane;
+      const float* pp = slot(i);
 #pragma unroll
       for (int t = 0; t < 8 * NT; ++t) v[j][t] = (i <= i_last && t < a.M) ? __ldcg(pp + t * 32) : 0.f;
     }
@@ -137,6 +150,30 @@ __device__ __forceinline__ void flush_block(const GemvArgs& a, const Range& R, i
 #pragma unroll
   for (int t = 0; t < 8 * NT; ++t)
     if (t < a.M) a.Y[(size_t)t * a.N + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
+}
+
+// The CTA is done: publish this warp's partials of split blocks p0 and p1
+// (the CTA's first and last block; -1 for none) and take their tickets; the
+// contributor that completes a block's count sums it and resets the ticket.
+template <int NT, bool BF16>
+__device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R, int warp, int lane, int p0, int p1) {
+  if (p0 < 0 && p1 < 0) return;
+  __threadfence();  // the partial stores above are visible before the tickets move
+  __syncwarp();
+  int last0 = 0, last1 = 0;
+  if (lane == 0) {
+    int* t0 = a.counters + p0 * kSliceWarps + warp;
+    int* t1 = a.counters + p1 * kSliceWarps + warp;
+    if (p0 >= 0) last0 = atomicAdd(t0, 1) == R.owner((long long)(p0 + 1) * a.G - 1) - R.owner((long long)p0 * a.G);
+    if (p1 >= 0) last1 = atomicAdd(t1, 1) == R.owner((long long)(p1 + 1) * a.G - 1) - R.owner((long long)p1 * a.G);
+    if (last0) *t0 = 0;  // ready for the next call
+    if (last1) *t1 = 0;
+    if (last0 || last1) __threadfence();
+  }
+  last0 = __shfl_sync(0xFFFFFFFFu, last0, 0);
+  last1 = __shfl_sync(0xFFFFFFFFu, last1, 0);
+  if (last0) reduce_block<NT, BF16>(a, R, warp, lane, p0);
+  if (last1) reduce_block<NT, BF16>(a, R, warp, lane, p1);
 }
 
 }  // namespace w4a16

@@ -52,21 +52,22 @@ constexpr int kWBox = 16 * 32 * 4;            // one slice: 16 word-rows x 32 co
 constexpr int kWBytes = kCW * kWBox;          // the unit's packed weights, 16 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// Shared memory: a ring of kStages weight stages (16 KB each, 1024-byte
+// Shared memory: a ring of STAGES weight stages (16 KB each, 1024-byte
 // aligned as the 128-byte swizzle of the weight boxes requires), then a ring
 // of as many side stages holding the rest of each unit (byte offsets within a
-// side stage below).
-constexpr int kStages = 4;  // a power of two: stage k % 4, phase (k / 4) % 2
+// side stage below).  The activations arrive raw ([8NT tokens][128 rows]) and
+// the helper rewrites them in place as B-operand pairs ([NT][4 steps][32
+// lanes] x 16 B, the same size).
 template <int NT>
 struct WsLayout {
+  static constexpr int STAGES = NT == 1 ? 5 : 4;     // as many as two CTAs per SM can hold
   static constexpr int CT = 0;                        // constants: [kCW][3][32] words
-  static constexpr int XR = CT + kCW * 3 * 32 * 4;    // raw activations: [8NT tokens][128 rows]
-  static constexpr int XP = XR + NT * 8 * 128 * 2;    // B-operand pairs: [NT][4 steps][32 lanes] x 16 B
-  static constexpr int SR = XP + NT * 4 * 32 * 16;    // raw scales: 256 x fp16
+  static constexpr int X = CT + kCW * 3 * 32 * 4;     // activations, raw then paired
+  static constexpr int SR = X + NT * 8 * 128 * 2;     // raw scales: 256 x fp16
   static constexpr int ZR = SR + kGemvCols * 2;       // raw zeros: 32 words
   static constexpr int SIDE = ZR + 32 * 4;            // a multiple of 128 bytes
-  static constexpr int SIDE_RING = kStages * kWBytes;
-  static constexpr int SMEM = 1024 + kStages * (kWBytes + SIDE);
+  static constexpr int SIDE_RING = STAGES * kWBytes;
+  static constexpr int SMEM = 1024 + STAGES * (kWBytes + SIDE);
   static constexpr uint32_t TX = kWBytes + NT * 8 * 128 * 2;  // TMA bytes per stage
 };
 static_assert(WsLayout<1>::SIDE % 128 == 0 && WsLayout<2>::SIDE % 128 == 0, "side stages keep TMA alignment");
@@ -114,7 +115,7 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
     cp_async_arrive_noinc(&full[s]);
   };
   auto issue_x = [&](int s, int g) {
-    if (lane == 0) tma_load_2d(smem + L::SIDE_RING + s * L::SIDE + L::XR, tmX, &full[s], g * 128, 0);
+    if (lane == 0) tma_load_2d(smem + L::SIDE_RING + s * L::SIDE + L::X, tmX, &full[s], g * 128, 0);
   };
   if (lane == 0) {
     prefetch_tmap(tmW);
@@ -123,7 +124,8 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   // The packed weights and their constants do not depend on the previous
   // kernel in the stream, so the first stages start before waiting for it;
   // the activations follow after griddep_wait.
-  const int n_first = nu < kStages ? nu : kStages;
+  constexpr int S = L::STAGES;
+  const int n_first = nu < S ? nu : S;
   int b = b0, g = g0;
   for (int k = 0; k < n_first; ++k) {
     issue_weights(k, b, g);
@@ -138,14 +140,14 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
     issue_x(k, gg);
     if (++gg == a.G) gg = 0;
   }
-  for (int k = kStages; k < nu; ++k) {
-    const int s = k & (kStages - 1);
-    // stage s was last filled for unit k - kStages: wait until it is released
-    if (!mbar_wait(&empty[s], (uint32_t)((k / kStages) & 1) ^ 1u, abort, a.dev_status, kWaitLimitNs)) {
+  int s = 0;
+  uint32_t ph = 0;  // parity of the release of stage s to wait for
+  for (int k = S; k < nu; ++k) {
+    // stage s was last filled for unit k - S: wait until it is released
+    if (!mbar_wait(&empty[s], ph, abort, a.dev_status, kWaitLimitNs)) {
       // let this CTA's copies in flight land before its shared memory goes away
       cp_async_wait_all();
-      for (int kk = k - kStages; kk < k; ++kk)
-        (void)mbar_drain(&full[kk & (kStages - 1)], (uint32_t)(kk / kStages) & 1u, kWaitLimitNs);
+      for (int kk = k - S; kk < k; ++kk) (void)mbar_drain(&full[kk % S], (uint32_t)(kk / S) & 1u, kWaitLimitNs);
       return;
     }
     issue_weights(s, b, g);
@@ -153,6 +155,10 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
     if (++g == a.G) {
       g = 0;
       ++b;
+    }
+    if (++s == S) {
+      s = 0;
+      ph ^= 1;
     }
   }
   cp_async_wait_all();
@@ -163,9 +169,10 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
                                           volatile int* abort, int nu, int lane) {
   using L = WsLayout<NT>;
   const int gl = lane >> 2, c = lane & 3;
+  int s = 0;
+  uint32_t ph = 0;
   for (int k = 0; k < nu; ++k) {
-    const int s = k & (kStages - 1);
-    if (!mbar_wait(&full[s], (uint32_t)(k / kStages) & 1u, abort, a.dev_status, kWaitLimitNs)) return;
+    if (!mbar_wait(&full[s], ph, abort, a.dev_status, kWaitLimitNs)) return;
     uint8_t* st = smem + L::SIDE_RING + s * L::SIDE;
     // constants of columns 8*lane .. 8*lane+7 of the unit: consumer warp
     // lane/4, slice columns 8*(lane%4) ..
@@ -196,19 +203,30 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
     ct[16] = make_uint4(k2[0], k2[1], k2[2], k2[3]);
     ct[17] = make_uint4(k2[4], k2[5], k2[6], k2[7]);
     // activation pairs: lane (gl, c) of every consumer reads, at step o, the
-    // pairs of token 8t + gl for word-row tile_row(c, o)
+    // pairs of token 8t + gl for word-row tile_row(c, o).  The 32 lanes'
+    // loads cover the raw tile exactly once, so it is rewritten in place.
+    uint4 xv[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int o = 0; o < 4; ++o)
+        xv[t][o] = *reinterpret_cast<const uint4*>(st + L::X + ((8 * t + gl) * 128 + 8 * tile_row(c, o)) * 2);
+    __syncwarp();
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int o = 0; o < 4; ++o) {
-        const int r = tile_row(c, o);
-        const uint4 xv = *reinterpret_cast<const uint4*>(st + L::XR + ((8 * t + gl) * 128 + 8 * r) * 2);
         uint32_t bf[4];
-        x_pairs(xv, bf);
-        *reinterpret_cast<uint4*>(st + L::XP + ((t * 4 + o) * 32 + lane) * 16) =
-            make_uint4(bf[0], bf[1], bf[2], bf[3]);
+        x_pairs(xv[t][o], bf);
+        *reinterpret_cast<uint4*>(st + L::X + ((t * 4 + o) * 32 + lane) * 16) = make_uint4(bf[0], bf[1], bf[2], bf[3]);
       }
+    // the next copy into this stage comes from the TMA unit
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(&ready[s]);
+    if (++s == L::STAGES) {
+      s = 0;
+      ph ^= 1;
+    }
   }
 }
 
@@ -226,7 +244,7 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
     const int r = tile_row(c, o);
     w_off[o] = (uint32_t)(warp * kWBox + r * 128 + ((gl ^ (r & 7)) << 4));
   }
-  const uint32_t x_off = (uint32_t)(L::XP + lane * 16);
+  const uint32_t x_off = (uint32_t)(L::X + lane * 16);
   const uint32_t c_off = (uint32_t)(L::CT + warp * 384 + gl * 16);
 
   // Y, the partial sums and the tickets may still be in use by the previous
@@ -237,7 +255,9 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
   // two accumulators per (token tile, column pair): even and odd steps o, so
   // that consecutive MMAs do not wait on each other
   float acc[NT][2][2][4];
-  int k = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  int p0 = -1, p1 = -1;  // split blocks whose tickets are still to be taken
   for (int b = b0, g = g0, left = nu; left > 0; ++b, g = 0) {
     const int n = a.G - g < left ? a.G - g : left;  // units of column block b
     left -= n;
@@ -250,9 +270,8 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[t][r][h][i] = 0.f;
 #pragma unroll 1
-    for (int j = 0; j < n; ++j, ++k) {
-      const int s = k & (kStages - 1);
-      if (!mbar_wait(&ready[s], (uint32_t)(k / kStages) & 1u, abort, a.dev_status, kWaitLimitNs)) return;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(&ready[s], ph, abort, a.dev_status, kWaitLimitNs)) return;
       const uint32_t ws_ = wbase + (uint32_t)(s * kWBytes);
       const uint32_t ss = sbase + (uint32_t)(s * L::SIDE);
       uint4 wv[4], xv[NT][4];
@@ -263,6 +282,12 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
 #pragma unroll
         for (int o = 0; o < 4; ++o) xv[t][o] = lds128(ss + x_off + (uint32_t)((t * 4 + o) * 512));
       const uint4 c0 = lds128(ss + c_off), c1 = lds128(ss + c_off + 128), c2 = lds128(ss + c_off + 256);
+      // One token tile: release the stage as soon as it has been read (the
+      // arrive orders the loads above before the producer's next copy into
+      // the stage).  Two tiles: the loaded values and the accumulators do not
+      // all fit in registers at once, so the loads stay interleaved with the
+      // arithmetic and the stage is released after it.
+      if (NT == 1) mbar_arrive(&empty[s]);
       const uint32_t k0[4] = {c0.x, c0.y, c0.z, c0.w}, k1[4] = {c1.x, c1.y, c1.z, c1.w},
                      k2[4] = {c2.x, c2.y, c2.z, c2.w};
 #pragma unroll
@@ -287,8 +312,11 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
           }
         }
       }
-      // every value read from the stage has gone into an MMA above
-      mbar_arrive(&empty[s]);
+      if (NT != 1) mbar_arrive(&empty[s]);
+      if (++s == L::STAGES) {
+        s = 0;
+        ph ^= 1;
+      }
     }
     float out[NT][2][4];
 #pragma unroll
@@ -297,8 +325,9 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
       for (int r = 0; r < 2; ++r)
 #pragma unroll
         for (int i = 0; i < 4; ++i) out[t][r][i] = acc[t][r][0][i] + acc[t][r][1][i];
-    flush_block<NT, BF16>(a, R, (int)blockIdx.x, b0, warp, lane, b, out);
+    if (store_block<NT, BF16>(a, R, (int)blockIdx.x, b0, warp, lane, b, out)) (b == b0 ? p0 : p1) = b;
   }
+  finish_blocks<NT, BF16>(a, R, warp, lane, p0, p1);
 }
 
 template <int NT, bool BF16>
@@ -306,7 +335,8 @@ __global__ void __launch_bounds__(kWsThreads, 2)
     gemv_ws_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemvArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kStages], ready[kStages], empty[kStages];
+  constexpr int S = WsLayout<NT>::STAGES;
+  __shared__ uint64_t full[S], ready[S], empty[S];
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int lane = threadIdx.x & 31;
@@ -318,7 +348,7 @@ __global__ void __launch_bounds__(kWsThreads, 2)
   const int b0 = (int)(u0 / a.G), g0 = (int)(u0 % a.G);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1 + 32);  // the producer's expect-tx arrival + its 32 lanes' cp.async arrivals
       mbar_init(&ready[s], 32);
       mbar_init(&empty[s], kCW * 32);

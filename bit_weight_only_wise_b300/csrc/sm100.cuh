@@ -55,10 +55,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for `parity` of `bar`.  Returns false (after raising *abort and the
-// status word) if the CTA is aborting or the limit passes.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* dev_status,
-                                          uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// status word) if the CTA is aborting or the limit passes.  The inline part is
+// a single poll; a wait that has to spin goes through the out-of-line loop
+// (try_wait itself suspends the thread for a while when the phase is not
+// complete), which keeps the polling code out of the callers' hot loops.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort, int* dev_status,
+                                            uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -71,6 +73,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* dev_status,
+                                          uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, dev_status, limit_ns);
 }
 
 // Teardown wait: ignores the abort flag (it is used after an abort, to let the
