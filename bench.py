@@ -16,6 +16,11 @@ shared generators, quantized on the GPU by the library's round-to-nearest
 kernel; the 64 layers are 64 distinct device copies of those four quantized
 linears (16.2 GB, far larger than the 126 MB L2, so no L2 flush is needed).
 
+* config sweep (``configs``): every workload's shapes and token counts (single
+  linear, decode sweep, act-order, Qwen shapes, NF4), each timed alone as a
+  CUDA graph rotating through weight copies that exceed 4x L2; us per call,
+  GB/s of algorithmic weight bytes, TFLOP/s and both roofline fractions.
+
 ``--impl reference`` times the CPU oracle instead (dequantize + fp64 product)
 on a bounded sample of the same workload on the host cores.
 """
@@ -170,6 +175,115 @@ def run_reference(args):
     return 0
 
 
+
+# ------------------------------------------------------------ config sweep
+# The five workloads' shapes and token counts, each timed on its own (CUDA
+# graph of calls that rotate through enough weight copies to exceed 4x L2).
+SWEEP = (
+    # (config, K, N, Ms, dtype, kind)
+    ("C1 single linear", 4096, 4096, (16,), "f16", "int4"),
+    ("C2 decode sweep qkv", 4096, 12288, (1, 4, 16), "bf16", "int4_salient"),
+    ("C2 decode sweep o", 4096, 4096, (1, 4, 16), "bf16", "int4_salient"),
+    ("C2 decode sweep gate_up", 4096, 22016, (1, 4, 16), "bf16", "int4_salient"),
+    ("C2 decode sweep down", 11008, 4096, (1, 4, 16), "bf16", "int4_salient"),
+    ("C3 act-order up", 8192, 28672, (1, 16, 64), "f16", "int4_act"),
+    ("C3 act-order down", 28672, 8192, (1, 16, 64), "f16", "int4_act"),
+    ("C4 Qwen qkv", 5120, 7168, (1, 256, 1024, 4096), "bf16", "int4"),
+    ("C4 Qwen o", 5120, 5120, (1, 256, 1024, 4096), "bf16", "int4"),
+    ("C4 Qwen gate_up", 5120, 55296, (1, 256, 1024, 4096), "bf16", "int4"),
+    ("C4 Qwen down", 27648, 5120, (1, 256, 1024, 4096), "bf16", "int4"),
+    ("C5 NF4", 8192, 8192, (1, 64, 1024), "bf16", "nf4"),
+)
+L2_BYTES = 126 * 2**20
+
+
+def sweep_weights(torch, w4, K, N, kind, seed, dev):
+    """Quantized weights of one linear, generated and quantized on the GPU:
+    N(0, 0.02) (C2: 1% of the K rows x10; C3: 0.01 * Student-t(5), drawn as
+    Z / sqrt(chi2_5 / 5) one column slab at a time; C3's g_idx is a seeded
+    permutation of the rows into groups of 128)."""
+    g = torch.Generator(device=dev).manual_seed(seed)
+    if kind == "int4_act":
+        W = torch.empty((K, N), dtype=torch.float32, device=dev)
+        for c0 in range(0, N, 4096):
+            c1 = min(N, c0 + 4096)
+            z = torch.randn((K, c1 - c0), generator=g, device=dev)
+            chi2 = sum(torch.randn((K, c1 - c0), generator=g, device=dev) ** 2 for _ in range(5))
+            W[:, c0:c1] = 0.01 * z / torch.sqrt(chi2 / 5)
+    else:
+        W = torch.randn((K, N), generator=g, device=dev) * 0.02
+        if kind == "int4_salient":
+            rows = torch.randperm(K, generator=g, device=dev)[: round(0.01 * K)]
+            W[rows] *= 10
+    if kind == "nf4":
+        qw, am = w4.nf4_quantize(W, w4.nf4_codebook(dev))
+        return (qw, am), K * N // 2 + (K // 64) * N * 4
+    qw, sc, qz = w4.quantize(W)
+    nbytes = int4_bytes(K, N)
+    if kind == "int4_act":
+        perm = torch.randperm(K, generator=g, device=dev)
+        gi = torch.empty(K, dtype=torch.int32, device=dev)
+        gi[perm] = (torch.arange(K, device=dev) // GROUP).to(torch.int32)
+        return (qw, sc, qz, gi), nbytes + 4 * K
+    return (qw, sc, qz), nbytes
+
+
+def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
+    out = []
+    for ci, (name, K, N, Ms, dt, kind) in enumerate(SWEEP):
+        w, nbytes = sweep_weights(torch, w4, K, N, kind, 1000 + ci, dev)
+        copies = max(2, -(-4 * L2_BYTES // nbytes))
+        sets = [w] + [tuple(t.clone() for t in w) for _ in range(copies - 1)]
+        cb = w4.nf4_codebook(dev) if kind == "nf4" else None
+        tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+        for M in Ms:
+            X = torch.randn((M, K), device=dev).to(tdt)
+            Y = torch.empty((M, N), dtype=tdt, device=dev)
+            ws = w4.workspace(M, N, K, dev)
+            # everything above was made on the default stream; the calls below
+            # run on a side stream
+            torch.cuda.synchronize()
+
+            def call(i):
+                t = sets[i % copies]
+                if kind == "nf4":
+                    w4.nf4_gemm(X, t[0], t[1], cb, out=Y, ws=ws)
+                else:
+                    w4.gemm(X, t[0], t[1], t[2], g_idx=t[3] if kind == "int4_act" else None, out=Y, ws=ws)
+
+            reps = max(copies, 8 if M >= 1024 else 20)
+            s = torch.cuda.Stream(dev)
+            with torch.cuda.stream(s):
+                for i in range(3):
+                    call(i)
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=s):
+                    for i in range(reps):
+                        call(i)
+            torch.cuda.synchronize()
+            gr.replay()
+            torch.cuda.synchronize()
+            cur = torch.cuda.current_stream(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n_rep = 3 if M >= 1024 else 5
+            e0.record(cur)
+            for _ in range(n_rep):
+                gr.replay()
+            e1.record(cur)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (n_rep * reps)
+            gbs = nbytes / us / 1e3
+            tf = 2 * M * N * K / us / 1e6
+            ent = {"config": name, "K": K, "N": N, "M": M, "dtype": dt, "us": round(us, 2), "GBs": round(gbs, 1),
+                   "TFLOPs": round(tf, 1), "hbm_frac": round(gbs / hbm_peak, 4), "tc_frac": round(tf / tc_peak, 4),
+                   "bound": "hbm" if M <= 16 else ("both" if M < 256 else "tensor")}
+            out.append(ent)
+            del gr, X, Y
+        del sets, w
+        torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------- GPU
 # the decode kernel's complete source: the ncu traffic figure in profiles/ is
 # used only while these files are unchanged since the capture
@@ -230,6 +344,7 @@ def run_gpu(args):
     xs = [activations(1, K, "bf16", 7 + i).to(dev) for i, (_, K, _) in enumerate(LINEARS)]
     ys = [torch.empty((1, N), dtype=torch.bfloat16, device=dev) for (_, _, N) in LINEARS]
     s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))  # the inputs were made on the default stream
     with torch.cuda.stream(s):
         wss = [w4.workspace(1, N, K, dev) for (_, K, N) in LINEARS]
         ws = max(wss, key=lambda t: -1 if t is None else t.numel())
@@ -334,6 +449,8 @@ def run_gpu(args):
         v, cores, sample = oracle_sample(args.cpu_seconds)
         cpu = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
 
+    sweep = None if args.no_sweep else config_sweep(torch, w4, dev, hbm_peak, tc_peak)
+
     traffic = traffic_from_profiles("gemv_ws_kernel")
     achieved = per_gpu  # algorithmic bytes per launch / mean launch time == stack bytes / step time
     line = {
@@ -383,6 +500,7 @@ def run_gpu(args):
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: pinned-host X -> device, 256 C-ABI calls through the Python binding, "
                        "outputs -> pinned host"},
+        "configs": sweep,
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -401,6 +519,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-config timing sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

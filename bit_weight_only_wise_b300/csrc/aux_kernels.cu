@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(256) dequant_int4_kernel(const uint32_t* __res
   } else {
     int gr[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) gr[r] = g_idx[8 * i + r];
+    for (int r = 0; r < 8; ++r) gr[r] = checked_group(g_idx[8 * i + r], K / group_size, nullptr);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t z[8], s[8];

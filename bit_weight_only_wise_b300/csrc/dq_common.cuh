@@ -87,6 +87,17 @@ __device__ __forceinline__ float hi16_to_f32(uint32_t v, bool bf16) {
   return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
 
+// An act-order map entry outside [0, G) would index past the scale and zero
+// arrays.  It is clamped into range (so nothing outside them is read) and
+// reported as W4A16_ERR_INVALID_ARG (1) through the caller's status word.
+__device__ __forceinline__ int checked_group(int gr, int G, int* dev_status) {
+  if ((unsigned)gr >= (unsigned)G) {
+    if (dev_status) atomicExch(dev_status, 1 /* W4A16_ERR_INVALID_ARG */);
+    gr = gr < 0 ? 0 : G - 1;
+  }
+  return gr;
+}
+
 // ---------------------------------------------------------------- INT4, fp16
 // Per-(group, column) constants for the fp16 route; each half of a register
 // may belong to a different (group, column), so act-order can mix them.

@@ -261,7 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kWords; ++i) {
           const int4 ga = __ldg(gp + 2 * i), gb = __ldg(gp + 2 * i + 1);
-          const int gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+          const int G = p.K / 128;
+          const int gr[8] = {checked_group(ga.x, G, p.dev_status), checked_group(ga.y, G, p.dev_status),
+                             checked_group(ga.z, G, p.dev_status), checked_group(ga.w, G, p.dev_status),
+                             checked_group(gb.x, G, p.dev_status), checked_group(gb.y, G, p.dev_status),
+                             checked_group(gb.z, G, p.dev_status), checked_group(gb.w, G, p.dev_status)};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t t0 = act_tab[gr[2 * j] * kBN + nl], t1 = act_tab[gr[2 * j + 1] * kBN + nl];

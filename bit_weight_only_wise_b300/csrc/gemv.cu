@@ -143,7 +143,10 @@ struct Dq<kInt4Act, BF16> {
     if (ok) {
       const int4 g0 = __ldg(reinterpret_cast<const int4*>(a.g_idx + row0));
       const int4 g1 = __ldg(reinterpret_cast<const int4*>(a.g_idx + row0 + 4));
-      const int gr[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const int gr[8] = {checked_group(g0.x, a.G, a.dev_status), checked_group(g0.y, a.G, a.dev_status),
+                         checked_group(g0.z, a.G, a.dev_status), checked_group(g0.w, a.G, a.dev_status),
+                         checked_group(g1.x, a.G, a.dev_status), checked_group(g1.y, a.G, a.dev_status),
+                         checked_group(g1.z, a.G, a.dev_status), checked_group(g1.w, a.G, a.dev_status)};
       const int col = col0 + c4;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {

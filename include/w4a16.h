@@ -80,12 +80,16 @@ typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
  * tensor-core kernel.
  *   group_size: 128.
  *   workspace: device scratch of at least w4a16_workspace_bytes(M, N, K)
- *     bytes, zero-filled by the caller before its first use; every call that
- *     completes leaves it zero-filled again.  May be NULL when that size is 0.
- *     Calls that run at the same time must not share a workspace.
+ *     bytes, zero-filled by the caller before its first use.  Its first part
+ *     holds the split-K tickets, which every call that completes leaves at
+ *     zero again; the rest is scratch for fp32 partial sums.  May be NULL when
+ *     that size is 0.  Calls that run at the same time must not share a
+ *     workspace.
  *   dev_status: NULL, or a device int the caller zeroes; a kernel whose
  *     bounded wait expires writes W4A16_ERR_TIMEOUT there and stops early
- *     (its Y is then undefined).
+ *     (its Y is then undefined); a g_idx entry outside [0, K/128) writes
+ *     W4A16_ERR_INVALID_ARG there (the entry is clamped into range, so no
+ *     memory outside the scale and zero arrays is read; Y is meaningless).
  */
 w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scales,
                         const uint32_t* qzeros, const int32_t* g_idx, void* Y,

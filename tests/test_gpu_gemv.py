@@ -162,3 +162,27 @@ def test_gemv_workspace_shared_across_shapes():
         assert_close(to_f64(Y), Y_ref, A, f"{K}x{N}")
         outs.append(Y)
     assert torch.equal(outs[0].view(torch.int16), outs[-1].view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [4, 64])
+def test_act_order_entry_out_of_range_is_reported(M):
+    # a g_idx entry outside [0, K/128) is clamped by the kernels (nothing
+    # outside the scale and zero arrays is read) and reported as INVALID_ARG
+    from synth import act_order_g_idx
+
+    K, N = 512, 256
+    W = gaussian_weights(K, N, 0.02, 5)
+    g_idx = act_order_g_idx(K, 128, 5)
+    qw, sc, qz, _, _ = int4.quantize_packed(W, 128, g_idx)
+    bad = g_idx.copy()
+    bad[5], bad[300] = K // 128 + 7, -3
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w4.gemm(activations(M, K, "bf16", 1).cuda(), to_dev_u32(qw), to_dev(sc), to_dev_u32(qz), g_idx=to_dev(bad),
+            dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == w4.ERR_INVALID_ARG
+    st.zero_()
+    w4.gemm(activations(M, K, "bf16", 1).cuda(), to_dev_u32(qw), to_dev(sc), to_dev_u32(qz), g_idx=to_dev(g_idx),
+            dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
