@@ -236,10 +236,20 @@ def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
         sets = [w] + [tuple(t.clone() for t in w) for _ in range(copies - 1)]
         cb = w4.nf4_codebook(dev) if kind == "nf4" else None
         tdt = torch.bfloat16 if dt == "bf16" else torch.float16
-        for M in Ms:
+        # act-order runs twice: on the g_idx map as stored, and prepacked
+        # (rows reordered by group once, before timing; X gathered per call)
+        runs = [(name, kind, sets)]
+        if kind == "int4_act":
+            packed = []
+            for t in sets:
+                q_sorted, perm = w4.act_order_prepack(t[0], t[3])
+                packed.append((q_sorted, t[1], t[2], perm))
+            runs.append((name + " (prepacked)", "int4_prepacked", packed))
+        for name, kind, sets, M in [(n, k, st, M) for (n, k, st) in runs for M in Ms]:
             X = torch.randn((M, K), device=dev).to(tdt)
             Y = torch.empty((M, N), dtype=tdt, device=dev)
             ws = w4.workspace(M, N, K, dev)
+            pws = w4.workspace(M, N, K, dev, nbytes=w4.prepacked_workspace_bytes(M, N, K))
             # everything above was made on the default stream; the calls below
             # run on a side stream
             torch.cuda.synchronize()
@@ -248,6 +258,8 @@ def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
                 t = sets[i % copies]
                 if kind == "nf4":
                     w4.nf4_gemm(X, t[0], t[1], cb, out=Y, ws=ws)
+                elif kind == "int4_prepacked":
+                    w4.gemm_prepacked(X, t[0], t[1], t[2], t[3], out=Y, ws=pws)
                 else:
                     w4.gemm(X, t[0], t[1], t[2], g_idx=t[3] if kind == "int4_act" else None, out=Y, ws=ws)
 
@@ -279,7 +291,7 @@ def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
                    "bound": "hbm" if M <= 16 else ("both" if M < 256 else "tensor")}
             out.append(ent)
             del gr, X, Y
-        del sets, w
+        del sets, w, runs
         torch.cuda.empty_cache()
     return out
 

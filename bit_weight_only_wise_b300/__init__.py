@@ -45,6 +45,9 @@ _SIGS = {
     "w4a16_quantize": [_vp, _i, _i, _i, _vp, _vp, _vp, _vp],
     "nf4_quantize": [_vp, _i, _i, _i, _vp, _vp, _vp, _vp],
     "w4a16_workspace_bytes": [_i, _i, _i],
+    "w4a16_act_order_prepack": [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp],
+    "w4a16_gemm_prepacked": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
+    "w4a16_prepacked_workspace_bytes": [_i, _i, _i],
     "w4a16_status_string": [_i],
 }
 for _name, _args in _SIGS.items():
@@ -52,6 +55,7 @@ for _name, _args in _SIGS.items():
     _fn.argtypes = _args
     _fn.restype = _i
 _lib.w4a16_workspace_bytes.restype = _sz
+_lib.w4a16_prepacked_workspace_bytes.restype = _sz
 _lib.w4a16_status_string.restype = ctypes.c_char_p
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -93,13 +97,15 @@ def workspace_bytes(M: int, N: int, K: int) -> int:
 _workspaces: dict = {}
 
 
-def workspace(M: int, N: int, K: int, device=None) -> torch.Tensor | None:
-    """A zero-initialised workspace big enough for (M, N, K), cached per device and stream.
+def workspace(M: int, N: int, K: int, device=None, nbytes: int | None = None) -> torch.Tensor | None:
+    """A zero-initialised workspace big enough for (M, N, K) (or ``nbytes``),
+    cached per device and stream.
 
     Calls on one stream run in order, so sharing one buffer between them is
-    safe; each stream gets its own.
+    safe; each stream gets its own.  Every layout starts with the split-K
+    tickets, which the calls leave at zero, so one buffer serves them all.
     """
-    n = workspace_bytes(M, N, K)
+    n = workspace_bytes(M, N, K) if nbytes is None else nbytes
     if n == 0:
         return None
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
@@ -163,6 +169,45 @@ def nf4_gemm(X, qweight, absmax, codebook, out=None, blocksize=NF4_BLOCK, ws=Non
     st = _lib.nf4_gemm(_ptr(X), _ptr(qweight), _ptr(absmax), _ptr(codebook), _ptr(Y), M, N, K, blocksize,
                        _DTYPES[X.dtype], _ptr(ws), nbytes, _ptr(dev_status), _stream(X.device))
     _check(st, "nf4_gemm")
+    return Y
+
+
+def act_order_prepack(qweight, g_idx, group_size=GROUP_SIZE, dev_status=None):
+    """One-time reorder of an act-order checkpoint: (qweight_sorted, perm) with
+    each group's rows contiguous; use with :func:`gemm_prepacked`.  A group
+    that does not hold exactly ``group_size`` rows is reported as
+    ERR_UNSUPPORTED through ``dev_status``."""
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    if g_idx.dtype != torch.int32 or g_idx.numel() != K:
+        raise ValueError("g_idx must be an int32 tensor of K entries")
+    q_sorted = torch.empty_like(qweight)
+    perm = torch.empty(K, dtype=torch.int32, device=qweight.device)
+    st = _lib.w4a16_act_order_prepack(_ptr(qweight), _ptr(g_idx), K, N, group_size, _ptr(q_sorted), _ptr(perm),
+                                      _ptr(dev_status), _stream(qweight.device))
+    _check(st, "w4a16_act_order_prepack")
+    return q_sorted, perm
+
+
+def prepacked_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_lib.w4a16_prepacked_workspace_bytes(M, N, K))
+
+
+def gemm_prepacked(X, qweight_sorted, scales, qzeros, perm, out=None, group_size=GROUP_SIZE, ws=None,
+                   dev_status=None):
+    """Y = X . W_hat for act-order weights prepacked by :func:`act_order_prepack`."""
+    K = qweight_sorted.shape[0] * 8
+    N = qweight_sorted.shape[1]
+    _check_x(X, K)
+    M = X.shape[0]
+    Y = _out(X, N, out)
+    need = prepacked_workspace_bytes(M, N, K)
+    if ws is None:
+        ws = workspace(M, N, K, X.device, nbytes=need)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _lib.w4a16_gemm_prepacked(_ptr(X), _ptr(qweight_sorted), _ptr(scales), _ptr(qzeros), _ptr(perm), _ptr(Y),
+                                   M, N, K, group_size, _DTYPES[X.dtype], _ptr(ws), nbytes, _ptr(dev_status),
+                                   _stream(X.device))
+    _check(st, "w4a16_gemm_prepacked")
     return Y
 
 

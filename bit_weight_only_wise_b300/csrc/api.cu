@@ -21,6 +21,7 @@ constexpr int kMaxK = 65535 * 8;  // word-rows index a grid dimension
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 bool ok_dtype(w4a16_dtype d) { return d == W4A16_F16 || d == W4A16_BF16; }
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
 w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
 
@@ -210,6 +211,51 @@ size_t w4a16_workspace_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (M <= W4A16_GEMV_MAX_M) return gemv_plan(M, N, K, kInt4).workspace_bytes;
   return 0;
+}
+
+w4a16_status w4a16_act_order_prepack(const uint32_t* qweight, const int32_t* g_idx, int K, int N, int group_size,
+                                     uint32_t* qweight_sorted, int32_t* perm, int* dev_status,
+                                     cudaStream_t stream) {
+  w4a16_status st = check_int4_shape(0, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(qweight) || !ok_ptr(g_idx) || !ok_ptr(qweight_sorted) || !ok_ptr(perm)) return W4A16_ERR_INVALID_ARG;
+  if (qweight_sorted == qweight) return W4A16_ERR_INVALID_ARG;  // rows are gathered: no in-place reorder
+  return from_cuda(launch_act_order_prepack(qweight, g_idx, K, N, group_size, qweight_sorted, perm, dev_status,
+                                            stream));
+}
+
+// [plain-kernel workspace, at least the ticket area | X with its columns in
+// sorted order]: the ticket area stays in front whatever M is, so a buffer
+// shared with the other entry points keeps its tickets
+static size_t prepacked_front_bytes(int M, int N, int K) {
+  const size_t plain = w4a16_workspace_bytes(M, N, K);
+  return align256(plain > kCountersBytes ? plain : kCountersBytes);
+}
+
+size_t w4a16_prepacked_workspace_bytes(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return prepacked_front_bytes(M, N, K) + align256((size_t)M * K * 2);
+}
+
+w4a16_status w4a16_gemm_prepacked(const void* X, const uint32_t* qweight_sorted, const void* scales,
+                                  const uint32_t* qzeros, const int32_t* perm, void* Y, int M, int N, int K,
+                                  int group_size, w4a16_dtype dtype, void* workspace, size_t workspace_bytes,
+                                  int* dev_status, cudaStream_t stream) {
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_int4_shape(M, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (M == 0 || N == 0) return W4A16_OK;
+  st = check_int4_ptrs(X, qweight_sorted, scales, qzeros, nullptr, Y);
+  if (st != W4A16_OK) return st;
+  if (!ok_ptr(perm) || !ok_ptr(workspace) || workspace_bytes < w4a16_prepacked_workspace_bytes(M, N, K))
+    return W4A16_ERR_INVALID_ARG;
+  const size_t plain = w4a16_workspace_bytes(M, N, K);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + prepacked_front_bytes(M, N, K));
+  cudaError_t e = launch_gather_columns(static_cast<const uint16_t*>(X), perm, M, K, Xp, stream);
+  if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  return w4a16_gemm(Xp, qweight_sorted, scales, qzeros, nullptr, Y, M, N, K, group_size, dtype,
+                    plain ? workspace : nullptr, plain, dev_status, stream);
 }
 
 const char* w4a16_status_string(w4a16_status status) {

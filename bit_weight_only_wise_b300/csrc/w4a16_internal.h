@@ -78,6 +78,12 @@ int gemm_tokens_per_cta(int M, bool act_order);
 bool gemm_act_order_fits(int K);
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st);
 
+// ------------------------------------------------------ act-order prepack
+cudaError_t launch_act_order_prepack(const uint32_t* qw, const int32_t* g_idx, int K, int N, int group_size,
+                                     uint32_t* qw_sorted, int32_t* perm, int* dev_status, cudaStream_t st);
+cudaError_t launch_gather_columns(const uint16_t* X, const int32_t* perm, int M, int K, uint16_t* out,
+                                  cudaStream_t st);
+
 // ------------------------------------------------------- standalone kernels
 cudaError_t launch_dequant_int4(const uint32_t* qw, const uint16_t* scales, const uint32_t* qz,
                                 const int32_t* g_idx, uint16_t* out, int K, int N, int group_size,

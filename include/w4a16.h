@@ -176,6 +176,47 @@ w4a16_status w4a16_gemv_noalloc(const void* X, const uint32_t* qweight, const vo
  * shape (0 when none is needed).  Pure host function. */
 size_t w4a16_workspace_bytes(int M, int N, int K);
 
+/*
+ * Act-order prepack, run once when a checkpoint is loaded.  With act-order
+ * ("GPTQ与bitsandbytes对比" GPTQ section, --act-order; "模型量化实践" §3.1,
+ * desc_act) the rows of one group are scattered over K.  This reorders them
+ * so that group g occupies rows [g*128, (g+1)*128), each group's rows keeping
+ * their original order:
+ *   perm[j]            = the original row of sorted row j
+ *   qweight_sorted row j = qweight row perm[j]          (same nibble packing)
+ * after which  Y = X . W_hat = X[:, perm] . W_hat_sorted  with plain groups
+ * (scales and qzeros are unchanged).  Every group must hold exactly
+ * group_size rows (GPTQ's layout); otherwise *dev_status (when not NULL)
+ * receives W4A16_ERR_UNSUPPORTED and the outputs are unspecified -- use the
+ * g_idx entry points for such maps.  Entries of g_idx outside [0, K/128) are
+ * never matched, so they show up the same way.
+ *   qweight_sorted: uint32 [K/8, N], not aliasing qweight; perm: int32 [K].
+ *   Both caller-owned device buffers, written asynchronously on `stream`.
+ */
+w4a16_status w4a16_act_order_prepack(const uint32_t* qweight, const int32_t* g_idx, int K, int N,
+                                     int group_size, uint32_t* qweight_sorted, int32_t* perm,
+                                     int* dev_status, cudaStream_t stream);
+
+/*
+ * Y = X . W_hat for act-order weights prepacked by w4a16_act_order_prepack:
+ * X's columns are gathered by perm into the workspace, then the plain-group
+ * kernels run (the decode kernel for M <= 16, the tensor-core kernel above),
+ * so act-order costs one gather of M*K values per call.  Arguments as
+ * w4a16_gemm, with perm in place of g_idx; workspace: at least
+ * w4a16_prepacked_workspace_bytes(M, N, K) bytes, zero-filled before its first
+ * use.  Its first part is laid out as w4a16_gemm's workspace (always at least
+ * the split-K ticket area, whatever M is, so one buffer can serve every entry
+ * point); the rest is scratch for the gathered X.  perm values outside
+ * [0, K) are clamped (no access outside X).
+ */
+w4a16_status w4a16_gemm_prepacked(const void* X, const uint32_t* qweight_sorted, const void* scales,
+                                  const uint32_t* qzeros, const int32_t* perm, void* Y, int M, int N,
+                                  int K, int group_size, w4a16_dtype dtype, void* workspace,
+                                  size_t workspace_bytes, int* dev_status, cudaStream_t stream);
+
+/* Bytes of workspace w4a16_gemm_prepacked needs.  Pure host function. */
+size_t w4a16_prepacked_workspace_bytes(int M, int N, int K);
+
 /* Static, human-readable text for a status code.  Pure host function. */
 const char* w4a16_status_string(w4a16_status status);
 

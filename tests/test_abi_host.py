@@ -28,7 +28,8 @@ def lib():
 def test_header_declares_expected_entry_points():
     names = _declared()
     for n in ("w4a16_gemm", "w4a16_gemv", "nf4_gemm", "w4a16_dequant", "nf4_dequant", "w4a16_quantize",
-              "nf4_quantize", "w4a16_workspace_bytes", "w4a16_status_string"):
+              "nf4_quantize", "w4a16_workspace_bytes", "w4a16_status_string", "w4a16_act_order_prepack",
+              "w4a16_gemm_prepacked", "w4a16_prepacked_workspace_bytes"):
         assert n in names
 
 
@@ -84,6 +85,14 @@ def test_validation_rejects_without_launch(lib):
     assert lib.nf4_dequant(16, 16, None, 16, 256, 64, 64, 0, None) == INV
     assert lib.w4a16_quantize(None, 256, 64, 128, 16, 16, 16, None) == INV
     assert lib.nf4_quantize(16, 256, 64, 64, None, 16, 16, None) == INV
+    # act-order prepack: no in-place reorder, group size, g_idx required
+    assert lib.w4a16_act_order_prepack(16, 16, 256, 64, 128, 16, 32, None, None) == INV  # aliasing
+    assert lib.w4a16_act_order_prepack(16, 16, 256, 64, 64, 32, 48, None, None) == UNS
+    assert lib.w4a16_act_order_prepack(16, None, 256, 64, 128, 32, 48, None, None) == INV
+    need = lib.w4a16_prepacked_workspace_bytes(4, 64, 256)
+    assert need >= 4 * 256 * 2
+    assert lib.w4a16_gemm_prepacked(16, 16, 16, 16, 16, 16, 4, 64, 256, 128, 1, 32, need - 1, None, None) == INV
+    assert lib.w4a16_gemm_prepacked(16, 16, 16, 16, None, 16, 4, 64, 256, 128, 1, 32, need, None, None) == INV
 
 
 def test_workspace_sizes_are_pure_and_bounded(lib):
