@@ -176,6 +176,25 @@ def run_reference(args):
 
 
 
+# ---------------------------------------------------- multi-rank (replicas)
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: every rank runs its own replica of the
+    workload, so the job takes as long as its slowest rank (no data-path
+    exchange between ranks; this is the only collective)."""
+    if dist is None:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(world: int, bytes_per_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank streamed over the slowest rank's time."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------ config sweep
 # The five workloads' shapes and token counts, each timed on its own (CUDA
 # graph of calls that rotate through enough weight copies to exceed 4x L2).
@@ -387,19 +406,14 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        ms = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = t.item()
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
     cur = torch.cuda.current_stream(dev)
     with ClockSampler(local) as clk:
         dec_ms = timed(g.replay, args.steps, args.warmup, cur)
     clocks = clk.summary()
     dec_step_ms = dec_ms / args.steps
-    value = world * STACK_BYTES * args.steps / (dec_ms * 1e-3) / 1e9
+    value = aggregate_gbs(world, STACK_BYTES, args.steps, dec_ms)
     per_gpu = STACK_BYTES / (dec_step_ms * 1e-3) / 1e9
     launches = args.steps * LAYERS * 4
 

@@ -152,16 +152,55 @@ __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, 
     if (t < a.M) a.Y[(size_t)t * a.N + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
 }
 
+// reduce_block for two blocks at M = 1 with every contributor's load of both
+// in flight at once (a warp that completes both of its blocks' counts)
+template <bool BF16>
+__device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Range& R, int warp, int lane, int b0,
+                                                     int b1) {
+  int first[2], last[2], sgf[2], col[2];
+  const int bs[2] = {b0, b1};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    first[h] = R.owner((long long)bs[h] * a.G);
+    last[h] = R.owner((long long)(bs[h] + 1) * a.G - 1);
+    sgf[h] = R.start(first[h]) == (long long)bs[h] * a.G ? 0 : 1;
+    col[h] = bs[h] * kGemvCols + warp * 32 + lane;
+  }
+  float sum[2] = {0.f, 0.f};
+  const int n = max(last[0] - first[0], last[1] - first[1]) + 1;
+  for (int j0 = 0; j0 < n; j0 += 8) {
+    float v[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = first[h] + j0 + j;
+        const float* pp =
+            a.partial + ((size_t)(i * 2 + (i == first[h] ? sgf[h] : 0)) * kSliceWarps + warp) * 32 + lane;
+        v[h][j] = (i <= last[h] && col[h] < a.N) ? __ldcg(pp) : 0.f;
+      }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum[h] += v[h][j];
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (col[h] < a.N) a.Y[col[h]] = (uint16_t)(pack2_rn(sum[h], 0.f, BF16) & 0xFFFFu);
+}
+
 // The CTA is done: publish this warp's partials of split blocks p0 and p1
 // (the CTA's first and last block; -1 for none) and take their tickets; the
 // contributor that completes a block's count sums it and resets the ticket.
 template <int NT, bool BF16>
 __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R, int warp, int lane, int p0, int p1) {
   if (p0 < 0 && p1 < 0) return;
-  __threadfence();  // the partial stores above are visible before the tickets move
+  // the warp barrier orders every lane's partial stores before lane 0's
+  // fence, whose release covers them before the tickets move
   __syncwarp();
   int last0 = 0, last1 = 0;
   if (lane == 0) {
+    __threadfence();
     int* t0 = a.counters + p0 * kSliceWarps + warp;
     int* t1 = a.counters + p1 * kSliceWarps + warp;
     if (p0 >= 0) last0 = atomicAdd(t0, 1) == R.owner((long long)(p0 + 1) * a.G - 1) - R.owner((long long)p0 * a.G);
@@ -172,6 +211,10 @@ __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R,
   }
   last0 = __shfl_sync(0xFFFFFFFFu, last0, 0);
   last1 = __shfl_sync(0xFFFFFFFFu, last1, 0);
+  if (last0 && last1 && a.M == 1) {  // both blocks: one round trip for the two
+    reduce_two_blocks_m1<BF16>(a, R, warp, lane, p0, p1);
+    return;
+  }
   if (last0) reduce_block<NT, BF16>(a, R, warp, lane, p0);
   if (last1) reduce_block<NT, BF16>(a, R, warp, lane, p1);
 }
