@@ -48,6 +48,7 @@ _SIGS = {
     "w4a16_act_order_prepack": [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp],
     "w4a16_gemm_prepacked": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
     "w4a16_prepacked_workspace_bytes": [_i, _i, _i],
+    "w4a16_selftest_wait_timeout": [_vp, ctypes.c_ulonglong, _vp],
     "w4a16_status_string": [_i],
 }
 for _name, _args in _SIGS.items():
@@ -209,6 +210,14 @@ def gemm_prepacked(X, qweight_sorted, scales, qzeros, perm, out=None, group_size
                                    _stream(X.device))
     _check(st, "w4a16_gemm_prepacked")
     return Y
+
+
+def selftest_wait_timeout(dev_status, limit_ns: int = 20_000_000):
+    """Run the bounded-wait self-test on ``dev_status``'s device: a wait on a
+    barrier nothing completes must end after ``limit_ns`` with ERR_TIMEOUT
+    written to ``dev_status``."""
+    st = _lib.w4a16_selftest_wait_timeout(_ptr(dev_status), limit_ns, _stream(dev_status.device))
+    _check(st, "w4a16_selftest_wait_timeout")
 
 
 def dequant(qweight, scales, qzeros, g_idx=None, dtype=torch.bfloat16, group_size=GROUP_SIZE):

@@ -217,6 +217,17 @@ w4a16_status w4a16_gemm_prepacked(const void* X, const uint32_t* qweight_sorted,
 /* Bytes of workspace w4a16_gemm_prepacked needs.  Pure host function. */
 size_t w4a16_prepacked_workspace_bytes(int M, int N, int K);
 
+/*
+ * Self-test of the bounded device-side wait that every pipeline wait in this
+ * library uses (no counterpart in the pages: a library diagnostic).  One warp
+ * waits on a barrier that nothing completes; after limit_ns (1 ns .. 10 s) of
+ * wall-clock time the wait gives up, writes W4A16_ERR_TIMEOUT to *dev_status
+ * and the kernel returns, so the caller can check that a stuck pipeline ends
+ * with a status rather than a hang and that the context stays usable.
+ * dev_status must not be NULL.
+ */
+w4a16_status w4a16_selftest_wait_timeout(int* dev_status, unsigned long long limit_ns, cudaStream_t stream);
+
 /* Static, human-readable text for a status code.  Pure host function. */
 const char* w4a16_status_string(w4a16_status status);
 

@@ -85,6 +85,10 @@ def test_validation_rejects_without_launch(lib):
     assert lib.nf4_dequant(16, 16, None, 16, 256, 64, 64, 0, None) == INV
     assert lib.w4a16_quantize(None, 256, 64, 128, 16, 16, 16, None) == INV
     assert lib.nf4_quantize(16, 256, 64, 64, None, 16, 16, None) == INV
+    # the wait self-test needs a status word and a limit in (0, 10 s]
+    assert lib.w4a16_selftest_wait_timeout(None, 1000, None) == INV
+    assert lib.w4a16_selftest_wait_timeout(16, 0, None) == INV
+    assert lib.w4a16_selftest_wait_timeout(16, 20 * 10**9, None) == INV
     # act-order prepack: no in-place reorder, group size, g_idx required
     assert lib.w4a16_act_order_prepack(16, 16, 256, 64, 128, 16, 32, None, None) == INV  # aliasing
     assert lib.w4a16_act_order_prepack(16, 16, 256, 64, 64, 32, 48, None, None) == UNS
