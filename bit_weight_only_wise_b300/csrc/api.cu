@@ -42,6 +42,12 @@ w4a16_status check_nf4_shape(int M, int N, int K, int blocksize) {
   return W4A16_OK;
 }
 
+w4a16_status check_gemm_workspace(const GemmSplit& sp, void* ws, size_t ws_bytes) {
+  if (sp.workspace_bytes == 0) return W4A16_OK;
+  if (!ok_ptr(ws) || ws_bytes < sp.workspace_bytes) return W4A16_ERR_INVALID_ARG;
+  return W4A16_OK;
+}
+
 w4a16_status check_workspace(const GemvPlan& p, void* ws, size_t ws_bytes) {
   if (p.workspace_bytes == 0) return W4A16_OK;
   if (!ok_ptr(ws) || ws_bytes < p.workspace_bytes) return W4A16_ERR_INVALID_ARG;
@@ -118,6 +124,8 @@ w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scal
     return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
                           dev_status, stream);
   if (g_idx && !gemm_act_order_fits(K)) return W4A16_ERR_UNSUPPORTED;
+  st = check_gemm_workspace(gemm_split_plan(M, N, K, g_idx != nullptr), workspace, workspace_bytes);
+  if (st != W4A16_OK) return st;
   GemmArgs a{};
   a.X = X;
   a.qw = qweight;
@@ -129,6 +137,8 @@ w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scal
   a.M = M;
   a.N = N;
   a.K = K;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   return from_cuda(launch_gemm_tc(a, dtype == W4A16_BF16, false, stream));
 }
 
@@ -150,6 +160,8 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
     a.codebook = codebook16;
     return from_cuda(launch_gemv_nf4(a, dtype == W4A16_BF16, stream));
   }
+  st = check_gemm_workspace(gemm_split_plan(M, N, K, false), workspace, workspace_bytes);
+  if (st != W4A16_OK) return st;
   GemmArgs a{};
   a.X = X;
   a.qw = qweight;
@@ -160,6 +172,8 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
   a.M = M;
   a.N = N;
   a.K = K;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   return from_cuda(launch_gemm_tc(a, dtype == W4A16_BF16, true, stream));
 }
 
@@ -210,7 +224,10 @@ w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const flo
 size_t w4a16_workspace_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (M <= W4A16_GEMV_MAX_M) return gemv_plan(M, N, K, kInt4).workspace_bytes;
-  return 0;
+  // the tensor-core kernel's split-K tiles; act-order uses a smaller token tile
+  const size_t a = gemm_split_plan(M, N, K, false).workspace_bytes;
+  const size_t b = gemm_split_plan(M, N, K, true).workspace_bytes;
+  return a > b ? a : b;
 }
 
 w4a16_status w4a16_act_order_prepack(const uint32_t* qweight, const int32_t* g_idx, int K, int N, int group_size,

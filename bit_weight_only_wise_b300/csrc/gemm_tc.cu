@@ -69,6 +69,7 @@ struct __align__(8) Bars {
   uint64_t d_full;
   uint32_t tmem_base;
   int abort;
+  int last;  // split-K: this CTA completes its tile's count
   float cb[16];
 };
 
@@ -86,6 +87,10 @@ constexpr int kActTableRowBytes = kBN * 4;  // one group: 128 columns x (scale |
 constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmParams {
+  float* partial;  // split-K: fp32 tiles [tile][split][BT][128]
+  int* counters;   // split-K: one ticket per tile
+  int splits;      // K ranges per output tile (1: no split)
+  int kb_per_split;
   const int32_t* g_idx;
   const uint16_t* scales;
   const uint32_t* qz;
@@ -120,7 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // fastest and the (then L2-resident) weights are shared across a wave.
   const int n0 = (p.token_fast ? blockIdx.y : blockIdx.x) * kBN;
   const int m0 = (p.token_fast ? blockIdx.x : blockIdx.y) * p.BT;
-  const int nkb = (p.K + kBK - 1) / kBK;
+  // Split-K: CTA z of a tile takes K blocks [kb0, kb0 + nkb) (group aligned)
+  const int kb_total = (p.K + kBK - 1) / kBK;
+  const int kb0 = (int)blockIdx.z * p.kb_per_split;
+  const int nkb = min(p.kb_per_split, kb_total - kb0);
   volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
@@ -170,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % kStages;
         if (!mbar_wait(&bars->empty[s], ((it / kStages) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) break;
         mbar_arrive_expect_tx(&bars->full[s], tx);
-        tma_load_2d(sx + s * kXStageBytes, &tmX, &bars->full[s], it * kBK, m0);
-        tma_load_2d(sw + s * (kWStageBytes / 4), &tmW, &bars->full[s], n0, it * (kBK / 8));
+        tma_load_2d(sx + s * kXStageBytes, &tmX, &bars->full[s], (kb0 + it) * kBK, m0);
+        tma_load_2d(sw + s * (kWStageBytes / 4), &tmW, &bars->full[s], n0, (kb0 + it) * (kBK / 8));
         issued = it + 1;
       }
       if (*abort) {
@@ -212,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per-group constants, with the next group's raw values fetched early
     uint32_t s_raw = 0, z_raw = 0, s_nxt = 0, z_nxt = 0;
     float am = 0.f, am_nxt = 0.f;
-    auto fetch = [&](int kb, uint32_t& s_out, uint32_t& z_out, float& am_out) {
-      if (!ok || kb >= nkb || FMT == kFmtInt4Act) return;
+    auto fetch = [&](int kb, uint32_t& s_out, uint32_t& z_out, float& am_out) {  // kb: absolute K block
+      if (!ok || kb >= kb0 + nkb || FMT == kFmtInt4Act) return;
       if (FMT == kFmtInt4) {
         const int grp = kb >> 1;  // 128-row groups, 64-row stages
         s_out = p.scales[(size_t)grp * p.N + n];
@@ -222,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         am_out = p.absmax[(size_t)kb * p.N + n];  // 64-row blocks == stages
       }
     };
-    fetch(0, s_raw, z_raw, am);
-    fetch(FMT == kFmtNF4 ? 1 : 2, s_nxt, z_nxt, am_nxt);
+    fetch(kb0, s_raw, z_raw, am);
+    fetch(kb0 + (FMT == kFmtNF4 ? 1 : 2), s_nxt, z_nxt, am_nxt);
     uint32_t zmix = dq_zmix_f16(z_raw), s2 = s_raw * 0x10001u;
     DqConstBF16 cbf = dq_const_bf16(z_raw, s_raw);
 
@@ -235,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_raw = s_nxt;
         z_raw = z_nxt;
         am = am_nxt;
-        fetch(FMT == kFmtNF4 ? it + 1 : it + 2, s_nxt, z_nxt, am_nxt);
+        fetch(kb0 + (FMT == kFmtNF4 ? it + 1 : it + 2), s_nxt, z_nxt, am_nxt);
         if (FMT == kFmtInt4) {
           if (BF16) cbf = dq_const_bf16(z_raw, s_raw);
           else {
@@ -257,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t regs[4 * kWords];
       if constexpr (FMT == kFmtInt4Act) {
         // every K row has its own group: rows 64*it + 8*(kWords*h + i) + 2j, +1
-        const int4* gp = reinterpret_cast<const int4*>(p.g_idx + it * kBK + 8 * kWords * h);
+        const int4* gp = reinterpret_cast<const int4*>(p.g_idx + (kb0 + it) * kBK + 8 * kWords * h);
 #pragma unroll
         for (int i = 0; i < kWords; ++i) {
           const int4 ga = __ldg(gp + 2 * i), gb = __ldg(gp + 2 * i + 1);
@@ -309,7 +317,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA in flight before TMEM is freed.
     const bool done = mbar_drain(&bars->d_full, 0, kDrainLimitNs);
     tc_fence_after();
-    if (done && !*abort) {
+    if (done && !*abort && p.splits > 1) {
+      // Split-K: this CTA's fp32 tile goes to the workspace; the CTA that
+      // completes the tile's ticket sums the splits in split order
+      // (deterministic) and writes Y.
+      const int part = p.BT / kParts;
+      const int tile = (int)(blockIdx.x + gridDim.x * blockIdx.y);
+      const size_t tile_floats = (size_t)p.BT * kBN;
+      float* mine = p.partial + ((size_t)tile * p.splits + blockIdx.z) * tile_floats;
+      for (int c = h * part; c < (h + 1) * part; c += 8) {
+        uint32_t v[8];
+        tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine[(size_t)(c + j) * kBN + nl] = __uint_as_float(v[j]);
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");  // the dequant warps only
+      if (dw == 0 && lane == 0) {
+        __threadfence();
+        const int last = atomicAdd(p.counters + tile, 1) == p.splits - 1;
+        if (last) {
+          p.counters[tile] = 0;  // ready for the next call
+          __threadfence();
+        }
+        bars->last = last;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+      if (bars->last && ok) {
+        const float* base = p.partial + (size_t)tile * p.splits * tile_floats;
+        for (int c = h * part; c < (h + 1) * part; c += 8) {
+          float acc[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+          for (int z = 0; z < p.splits; ++z) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __ldcg(base + (size_t)z * tile_floats + (size_t)(c + j) * kBN + nl);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += v[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int m = m0 + c + j;
+            if (m < p.M) p.Y[(size_t)m * p.N + n] = (uint16_t)(pack2_rn(acc[j], 0.f, BF16) & 0xFFFFu);
+          }
+        }
+      }
+    } else if (done && !*abort) {
       const int part = p.BT / kParts;  // tokens per warp, a multiple of 8
       for (int c = h * part; c < (h + 1) * part; c += 8) {
         uint32_t v[8];
@@ -356,6 +410,27 @@ cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const Gemm
 
 }  // namespace
 
+// Split-K plan: when the output tiles do not fill one wave of the SMs, each
+// tile's K range is cut into `splits` group-aligned parts, as many as keep
+// every part's CTA in the first wave and every part at least 8 K blocks long.
+GemmSplit gemm_split_plan(int M, int N, int K, bool act_order) {
+  GemmSplit sp{};
+  sp.BT = gemm_tokens_per_cta(M, act_order);
+  const int tiles = ((N + kBN - 1) / kBN) * ((M + sp.BT - 1) / sp.BT);
+  const int kb_total = (K + kBK - 1) / kBK;
+  int splits = tiles > 0 ? kNumSMs / tiles : 1;
+  if (splits > kb_total / 8) splits = kb_total / 8;
+  if (splits < 1) splits = 1;
+  int kb_per = (kb_total + splits - 1) / splits;
+  kb_per += kb_per & 1;  // whole 128-row groups
+  sp.splits = (kb_total + kb_per - 1) / kb_per;
+  sp.kb_per_split = kb_per;
+  sp.tiles = tiles;
+  sp.workspace_bytes =
+      sp.splits > 1 ? kCountersBytes + (size_t)tiles * sp.splits * sp.BT * kBN * sizeof(float) : 0;
+  return sp;
+}
+
 int gemm_tokens_per_cta(int M, bool act_order) {
   const int cap = act_order ? max_bt<kFmtInt4Act>() : kMaxBT;
   if (M >= cap) return cap;
@@ -391,9 +466,17 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   p.K = a.K;
   p.BT = BT;
   p.idesc = sm100::idesc_f16(bf16, kBN, BT);
+  const GemmSplit sp = gemm_split_plan(a.M, a.N, a.K, act);
+  p.splits = sp.splits;
+  p.kb_per_split = sp.kb_per_split;
+  if (sp.splits > 1) {
+    if (!a.workspace || a.workspace_bytes < sp.workspace_bytes) return cudaErrorInvalidValue;
+    p.counters = static_cast<int*>(a.workspace);
+    p.partial = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + kCountersBytes);
+  }
   const unsigned col_tiles = (a.N + kBN - 1) / kBN, tok_tiles = (a.M + BT - 1) / BT;
   p.token_fast = (size_t)a.K * a.N / 2 > (size_t)64 << 20;
-  dim3 grid = p.token_fast ? dim3(tok_tiles, col_tiles) : dim3(col_tiles, tok_tiles);
+  dim3 grid = p.token_fast ? dim3(tok_tiles, col_tiles, sp.splits) : dim3(col_tiles, tok_tiles, sp.splits);
   if (nf4) return bf16 ? launch_tc<kFmtNF4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtNF4, false>(tmX, tmW, p, grid, st);
   if (act)
     return bf16 ? launch_tc<kFmtInt4Act, true>(tmX, tmW, p, grid, st)

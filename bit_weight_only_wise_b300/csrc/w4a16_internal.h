@@ -70,10 +70,21 @@ struct GemmArgs {
   uint16_t* Y;
   int* dev_status;
   int M, N, K;
+  void* workspace;  // split-K tickets and partial tiles (see gemm_split_plan)
+  size_t workspace_bytes;
 };
 
 // Tokens per CTA (the MMA's N) the tensor-core kernel uses for M tokens.
 int gemm_tokens_per_cta(int M, bool act_order);
+// Split-K plan of the tensor-core kernel for a shape (pure function).
+struct GemmSplit {
+  int BT;
+  int tiles;
+  int splits;
+  int kb_per_split;
+  size_t workspace_bytes;  // 0 when not split
+};
+GemmSplit gemm_split_plan(int M, int N, int K, bool act_order);
 // Whether the act-order variant's per-CTA (scale, zero) table fits for this K.
 bool gemm_act_order_fits(int K);
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st);

@@ -77,7 +77,8 @@ typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
 /*
  * Y = X . W_hat for the INT4 format, any M >= 0.  Dispatches on M: M <= 16
  * runs the split-K decode kernel (as w4a16_gemv), larger M the tcgen05
- * tensor-core kernel.
+ * tensor-core kernel, which also splits K when its output tiles alone would
+ * leave SMs idle (fp32 partial tiles summed in a fixed order: deterministic).
  *   group_size: 128.
  *   workspace: device scratch of at least w4a16_workspace_bytes(M, N, K)
  *     bytes, zero-filled by the caller before its first use.  Its first part

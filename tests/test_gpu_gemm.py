@@ -172,3 +172,21 @@ def test_gemm_act_order_full_size_m64(K, N):
     assert st.item() == 0
     Y_ref, A = int4_expected(W, X.double().numpy(), wl.dtype, cols, g_idx)
     assert_close(to_f64(Y)[:, cols], Y_ref, A, f"act-order {K}x{N} M=64")
+
+
+def test_gemm_split_k_is_deterministic_and_matches():
+    # 256 tokens over 5120 x 5120: 40 output tiles leave most SMs idle, so the
+    # kernel splits K; the partial tiles are summed in a fixed order
+    K, N, M = 5120, 5120, 256
+    W = gaussian_weights(K, N, 0.02, 21)
+    qw, sc, qz = w4.quantize(to_dev(W))
+    assert w4.workspace_bytes(M, N, K) > 0  # the split plan needs partial tiles
+    X = activations(M, K, "bf16", 21).cuda()
+    Y1 = w4.gemm(X, qw, sc, qz)
+    Y2 = w4.gemm(X, qw, sc, qz)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    rows = _sample_rows(M)
+    cols = sample_columns(N)
+    Y_ref, A = int4_expected(W, X.cpu().double().numpy()[rows], "bf16", cols)
+    assert_close(to_f64(Y1)[np.ix_(rows, cols)], Y_ref, A, "split-K 5120x5120 M=256")
