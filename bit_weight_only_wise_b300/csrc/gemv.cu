@@ -458,7 +458,8 @@ cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st) {
   return a.g_idx ? launch_gemv<kInt4Act>(a, bf16, st) : launch_gemv_ws_int4(a, bf16, st);
 }
 
-cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st) { return launch_gemv<kNF4>(a, bf16, st); }
+// NF4 runs on the warp-specialized kernel as well (gemv_ws.cu)
+cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st) { return launch_gemv_ws_nf4(a, bf16, st); }
 
 GemvPlan gemv_plan(int M, int N, int K, int fmt) {
   GemvPlan p{};

@@ -61,14 +61,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 template <int NT>
 struct WsLayout {
   static constexpr int STAGES = NT == 1 ? 5 : 4;     // as many as two CTAs per SM can hold
-  static constexpr int CT = 0;                        // constants: [kCW][3][32] words
+  static constexpr int CT = 0;                        // INT4 constants: [kCW][3][32] words
+  static constexpr int AM = 0;                        // NF4 absmax: [2 blocks][256 columns] fp32
   static constexpr int X = CT + kCW * 3 * 32 * 4;     // activations, raw then paired
   static constexpr int SR = X + NT * 8 * 128 * 2;     // raw scales: 256 x fp16
   static constexpr int ZR = SR + kGemvCols * 2;       // raw zeros: 32 words
   static constexpr int SIDE = ZR + 32 * 4;            // a multiple of 128 bytes
   static constexpr int SIDE_RING = STAGES * kWBytes;
   static constexpr int SMEM = 1024 + STAGES * (kWBytes + SIDE);
-  static constexpr uint32_t TX = kWBytes + NT * 8 * 128 * 2;  // TMA bytes per stage
+  static constexpr uint32_t TX = kWBytes + NT * 8 * 128 * 2;  // TMA bytes per stage (INT4)
+  static constexpr uint32_t TX_NF4 = TX + 2 * kGemvCols * 4;    // + the unit's absmax
 };
 static_assert(WsLayout<1>::SIDE % 128 == 0 && WsLayout<2>::SIDE % 128 == 0, "side stages keep TMA alignment");
 
@@ -92,27 +94,33 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // ------------------------------------------------------------------ roles
-template <int NT>
-__device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtensorMap* tmX, const GemvArgs& a,
-                                            uint8_t* smem, uint64_t* full, uint64_t* empty, volatile int* abort,
-                                            int nu, int b0, int g0, int lane) {
+template <int NT, int FMT>
+__device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmA,
+                                            const GemvArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                            volatile int* abort, int nu, int b0, int g0, int lane) {
   using L = WsLayout<NT>;
   const uint32_t side0 = smem_u32(smem) + L::SIDE_RING;
   const int nw = a.N >> 3;  // zero words per row
-  // weights, scales and zeros of unit (b, g) into stage s
+  // weights and their group metadata for unit (b, g) into stage s: INT4
+  // scales and zeros by cp.async, NF4 absmax (the unit's two 64-row blocks)
+  // by TMA
   auto issue_weights = [&](int s, int b, int g) {
-    if (lane == 0) mbar_arrive_expect_tx(&full[s], L::TX);
+    if (lane == 0) mbar_arrive_expect_tx(&full[s], FMT == kNF4 ? L::TX_NF4 : L::TX);
     __syncwarp();
     if (lane < kCW)
       tma_load_2d(smem + s * kWBytes + lane * kWBox, tmW, &full[s], b * kGemvCols + lane * 32, g * 16);
-    const uint32_t side = side0 + s * L::SIDE;
-    const int col = b * kGemvCols + 8 * lane;
-    const bool sv = col < a.N;
-    cp_async_16(side + L::SR + 16 * lane, sv ? a.scales + (size_t)g * a.N + col : a.scales, sv);
-    const int zc = b * 32 + lane;
-    const bool zv = zc < nw;
-    cp_async_4(side + L::ZR + 4 * lane, zv ? a.qz + (size_t)g * nw + zc : a.qz, zv);
-    cp_async_arrive_noinc(&full[s]);
+    if constexpr (FMT == kNF4) {
+      if (lane == kCW) tma_load_2d(smem + L::SIDE_RING + s * L::SIDE + L::AM, tmA, &full[s], b * kGemvCols, g * 2);
+    } else {
+      const uint32_t side = side0 + s * L::SIDE;
+      const int col = b * kGemvCols + 8 * lane;
+      const bool sv = col < a.N;
+      cp_async_16(side + L::SR + 16 * lane, sv ? a.scales + (size_t)g * a.N + col : a.scales, sv);
+      const int zc = b * 32 + lane;
+      const bool zv = zc < nw;
+      cp_async_4(side + L::ZR + 4 * lane, zv ? a.qz + (size_t)g * nw + zc : a.qz, zv);
+      cp_async_arrive_noinc(&full[s]);
+    }
   };
   auto issue_x = [&](int s, int g) {
     if (lane == 0) tma_load_2d(smem + L::SIDE_RING + s * L::SIDE + L::X, tmX, &full[s], g * 128, 0);
@@ -120,6 +128,7 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   if (lane == 0) {
     prefetch_tmap(tmW);
     prefetch_tmap(tmX);
+    if (FMT == kNF4) prefetch_tmap(tmA);
   }
   // The packed weights and their constants do not depend on the previous
   // kernel in the stream, so the first stages start before waiting for it;
@@ -164,7 +173,7 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   cp_async_wait_all();
 }
 
-template <int NT, bool BF16>
+template <int NT, int FMT, bool BF16>
 __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint64_t* full, uint64_t* ready,
                                           volatile int* abort, int nu, int lane) {
   using L = WsLayout<NT>;
@@ -174,34 +183,36 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
   for (int k = 0; k < nu; ++k) {
     if (!mbar_wait(&full[s], ph, abort, a.dev_status, kWaitLimitNs)) return;
     uint8_t* st = smem + L::SIDE_RING + s * L::SIDE;
-    // constants of columns 8*lane .. 8*lane+7 of the unit: consumer warp
-    // lane/4, slice columns 8*(lane%4) ..
-    const uint4 sv = *reinterpret_cast<const uint4*>(st + L::SR + 16 * lane);
-    const uint32_t zw = *reinterpret_cast<const uint32_t*>(st + L::ZR + 4 * lane);
-    const uint32_t sb[8] = {sv.x, sv.x >> 16, sv.y, sv.y >> 16, sv.z, sv.z >> 16, sv.w, sv.w >> 16};
-    uint32_t k0[8], k1[8], k2[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t z = (zw >> (4 * j)) & 0xFu;
-      if (BF16) {
-        const DqConstBF16 q = dq_const_bf16(z, sb[j] & 0xFFFFu);
-        k0[j] = q.z;
-        k1[j] = q.s_hi;
-        k2[j] = q.s_lo;
-      } else {
-        const DqConstF16 q = dq_const_f16(z, sb[j] & 0xFFFFu);
-        k0[j] = q.z_lo;
-        k1[j] = q.z_hi;
-        k2[j] = q.s;
+    if constexpr (FMT == kInt4) {
+      // constants of columns 8*lane .. 8*lane+7 of the unit: consumer warp
+      // lane/4, slice columns 8*(lane%4) ..
+      const uint4 sv = *reinterpret_cast<const uint4*>(st + L::SR + 16 * lane);
+      const uint32_t zw = *reinterpret_cast<const uint32_t*>(st + L::ZR + 4 * lane);
+      const uint32_t sb[8] = {sv.x, sv.x >> 16, sv.y, sv.y >> 16, sv.z, sv.z >> 16, sv.w, sv.w >> 16};
+      uint32_t k0[8], k1[8], k2[8];
+  #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t z = (zw >> (4 * j)) & 0xFu;
+        if (BF16) {
+          const DqConstBF16 q = dq_const_bf16(z, sb[j] & 0xFFFFu);
+          k0[j] = q.z;
+          k1[j] = q.s_hi;
+          k2[j] = q.s_lo;
+        } else {
+          const DqConstF16 q = dq_const_f16(z, sb[j] & 0xFFFFu);
+          k0[j] = q.z_lo;
+          k1[j] = q.z_hi;
+          k2[j] = q.s;
+        }
       }
+      uint4* ct = reinterpret_cast<uint4*>(st + L::CT) + (lane >> 2) * 24 + (lane & 3) * 2;
+      ct[0] = make_uint4(k0[0], k0[1], k0[2], k0[3]);
+      ct[1] = make_uint4(k0[4], k0[5], k0[6], k0[7]);
+      ct[8] = make_uint4(k1[0], k1[1], k1[2], k1[3]);
+      ct[9] = make_uint4(k1[4], k1[5], k1[6], k1[7]);
+      ct[16] = make_uint4(k2[0], k2[1], k2[2], k2[3]);
+      ct[17] = make_uint4(k2[4], k2[5], k2[6], k2[7]);
     }
-    uint4* ct = reinterpret_cast<uint4*>(st + L::CT) + (lane >> 2) * 24 + (lane & 3) * 2;
-    ct[0] = make_uint4(k0[0], k0[1], k0[2], k0[3]);
-    ct[1] = make_uint4(k0[4], k0[5], k0[6], k0[7]);
-    ct[8] = make_uint4(k1[0], k1[1], k1[2], k1[3]);
-    ct[9] = make_uint4(k1[4], k1[5], k1[6], k1[7]);
-    ct[16] = make_uint4(k2[0], k2[1], k2[2], k2[3]);
-    ct[17] = make_uint4(k2[4], k2[5], k2[6], k2[7]);
     // activation pairs: lane (gl, c) of every consumer reads, at step o, the
     // pairs of token 8t + gl for word-row tile_row(c, o).  The 32 lanes'
     // loads cover the raw tile exactly once, so it is rewritten in place.
@@ -230,10 +241,10 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
   }
 }
 
-template <int NT, bool BF16>
-__device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, uint8_t* smem, uint64_t* ready,
-                                            uint64_t* empty, volatile int* abort, int nu, int b0, int g0, int warp,
-                                            int lane) {
+template <int NT, int FMT, bool BF16>
+__device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, uint8_t* smem, const float* cbk,
+                                            uint64_t* ready, uint64_t* empty, volatile int* abort, int nu, int b0,
+                                            int g0, int warp, int lane) {
   using L = WsLayout<NT>;
   const int gl = lane >> 2, c = lane & 3;
   const uint32_t wbase = smem_u32(smem);
@@ -246,6 +257,7 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
   }
   const uint32_t x_off = (uint32_t)(L::X + lane * 16);
   const uint32_t c_off = (uint32_t)(L::CT + warp * 384 + gl * 16);
+  const uint32_t am_off = (uint32_t)(L::AM + (warp * 32 + 4 * gl) * 4);  // NF4: this lane's 4 columns
 
   // Y, the partial sums and the tickets may still be in use by the previous
   // kernel in the stream
@@ -281,7 +293,10 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
       for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int o = 0; o < 4; ++o) xv[t][o] = lds128(ss + x_off + (uint32_t)((t * 4 + o) * 512));
-      const uint4 c0 = lds128(ss + c_off), c1 = lds128(ss + c_off + 128), c2 = lds128(ss + c_off + 256);
+      // INT4: the columns' packed constants; NF4: their two blocks' absmax
+      const uint4 c0 = lds128(ss + (FMT == kNF4 ? am_off : c_off));
+      const uint4 c1 = lds128(ss + (FMT == kNF4 ? am_off + kGemvCols * 4 : c_off + 128));
+      const uint4 c2 = FMT == kNF4 ? c1 : lds128(ss + c_off + 256);
       // One token tile: release the stage as soon as it has been read (the
       // arrive orders the loads above before the producer's next copy into
       // the stage).  Two tiles: the loaded values and the accumulators do not
@@ -296,7 +311,12 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           uint32_t pa[4], pb[4];
-          if (BF16) {
+          if constexpr (FMT == kNF4) {
+            // word-row tile_row(c, o) lies in the unit's 64-row block o & 1
+            const uint32_t* am = (o & 1) ? k1 : k0;
+            dq_word_nf4<BF16>(wd[2 * rr], cbk, __uint_as_float(am[2 * rr]), pa);
+            dq_word_nf4<BF16>(wd[2 * rr + 1], cbk, __uint_as_float(am[2 * rr + 1]), pb);
+          } else if (BF16) {
             dq_word_bf16(wd[2 * rr], DqConstBF16{k0[2 * rr], k1[2 * rr], k2[2 * rr]}, pa);
             dq_word_bf16(wd[2 * rr + 1], DqConstBF16{k0[2 * rr + 1], k1[2 * rr + 1], k2[2 * rr + 1]}, pb);
           } else {
@@ -330,14 +350,15 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
   finish_blocks<NT, BF16>(a, R, warp, lane, p0, p1);
 }
 
-template <int NT, bool BF16>
+template <int NT, int FMT, bool BF16>
 __global__ void __launch_bounds__(kWsThreads, 2)
     gemv_ws_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const GemvArgs a) {
+                   const __grid_constant__ CUtensorMap tmA, const GemvArgs a) {
   extern __shared__ uint8_t smem_raw[];
   constexpr int S = WsLayout<NT>::STAGES;
   __shared__ uint64_t full[S], ready[S], empty[S];
   __shared__ int abort_flag;
+  __shared__ float s_cb[16];  // NF4 codebook
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -349,25 +370,27 @@ __global__ void __launch_bounds__(kWsThreads, 2)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + 32);  // the producer's expect-tx arrival + its 32 lanes' cp.async arrivals
+      // the producer's expect-tx arrival (+ INT4: its 32 lanes' cp.async arrivals)
+      mbar_init(&full[s], FMT == kNF4 ? 1 : 1 + 32);
       mbar_init(&ready[s], 32);
       mbar_init(&empty[s], kCW * 32);
     }
     abort_flag = 0;
     fence_mbar_init();
   }
+  if (FMT == kNF4 && threadIdx.x < 16) s_cb[threadIdx.x] = a.codebook[threadIdx.x];
   __syncthreads();
   volatile int* abort = &abort_flag;
   if (warp == kProducer)
-    ws_producer<NT>(&tmW, &tmX, a, smem, full, empty, abort, nu, b0, g0, lane);
+    ws_producer<NT, FMT>(&tmW, &tmX, &tmA, a, smem, full, empty, abort, nu, b0, g0, lane);
   else if (warp == kHelper)
-    ws_helper<NT, BF16>(a, smem, full, ready, abort, nu, lane);
+    ws_helper<NT, FMT, BF16>(a, smem, full, ready, abort, nu, lane);
   else
-    ws_consumer<NT, BF16>(a, R, smem, ready, empty, abort, nu, b0, g0, warp, lane);
+    ws_consumer<NT, FMT, BF16>(a, R, smem, s_cb, ready, empty, abort, nu, b0, g0, warp, lane);
 }
 
-template <int NT, bool BF16>
-cudaError_t launch_ws(const CUtensorMap& tmW, const GemvArgs& a, cudaStream_t st) {
+template <int NT, int FMT, bool BF16>
+cudaError_t launch_ws(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemvArgs& a, cudaStream_t st) {
   using L = WsLayout<NT>;
   CUtensorMap tmX;  // X [M, K], boxes of 128 rows x 8*NT tokens
   if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.X, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 128,
@@ -375,10 +398,10 @@ cudaError_t launch_ws(const CUtensorMap& tmW, const GemvArgs& a, cudaStream_t st
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_ws_kernel<NT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemv_ws_kernel<NT, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr = true;
@@ -393,18 +416,31 @@ cudaError_t launch_ws(const CUtensorMap& tmW, const GemvArgs& a, cudaStream_t st
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_ws_kernel<NT, BF16>, tmW, tmX, a);
+  return cudaLaunchKernelEx(&cfg, gemv_ws_kernel<NT, FMT, BF16>, tmW, tmX, tmA, a);
 }
 
 }  // namespace
 
-cudaError_t launch_gemv_ws_int4(const GemvArgs& a, bool bf16, cudaStream_t st) {
+template <int FMT>
+cudaError_t launch_gemv_ws(const GemvArgs& a, bool bf16, cudaStream_t st) {
   CUtensorMap tmW;  // packed weights [K/8, N] words, boxes of 16 word-rows x 32 columns
   if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.qw, (uint64_t)a.N, (uint64_t)(a.K / 8), (uint64_t)a.N * 4, 32,
                  16, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (a.M <= 8) return bf16 ? launch_ws<1, true>(tmW, a, st) : launch_ws<1, false>(tmW, a, st);
-  return bf16 ? launch_ws<2, true>(tmW, a, st) : launch_ws<2, false>(tmW, a, st);
+  CUtensorMap tmA = tmW;  // NF4 absmax [K/64, N] fp32, boxes of 2 blocks x 256 columns
+  if (FMT == kNF4 && !encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.absmax, (uint64_t)a.N, (uint64_t)(a.K / 64),
+                                (uint64_t)a.N * 4, kGemvCols, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (a.M <= 8) return bf16 ? launch_ws<1, FMT, true>(tmW, tmA, a, st) : launch_ws<1, FMT, false>(tmW, tmA, a, st);
+  return bf16 ? launch_ws<2, FMT, true>(tmW, tmA, a, st) : launch_ws<2, FMT, false>(tmW, tmA, a, st);
+}
+
+cudaError_t launch_gemv_ws_int4(const GemvArgs& a, bool bf16, cudaStream_t st) {
+  return launch_gemv_ws<kInt4>(a, bf16, st);
+}
+
+cudaError_t launch_gemv_ws_nf4(const GemvArgs& a, bool bf16, cudaStream_t st) {
+  return launch_gemv_ws<kNF4>(a, bf16, st);
 }
 
 }  // namespace w4a16

@@ -18,7 +18,7 @@ enum GemvFmt { kInt4 = 0, kInt4Act = 1, kNF4 = 2 };
 // persistent grid: CTAs resident per SM, by token tiles (M <= 8: one tile of
 // 8 tokens) and format (register and shared-memory budget of each variant)
 constexpr int kGemvMaxCTAsPerSM = 3;
-constexpr int gemv_ctas_per_sm(int M, int fmt) { return fmt == kInt4 ? 2 : M <= 8 ? 3 : 2; }
+constexpr int gemv_ctas_per_sm(int M, int fmt) { return fmt != kInt4Act ? 2 : M <= 8 ? 3 : 2; }
 // The workspace starts with a fixed-size area of split-K tickets (one int per
 // 32-column slice) and the fp32 partial sums follow it.  The area's size does
 // not depend on the shape, so partial sums of one call never land where a
@@ -54,8 +54,9 @@ struct GemvArgs {
 };
 
 cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st);
-// plain-group INT4 decode on the warp-specialized kernel
+// plain-group INT4 and NF4 decode on the warp-specialized kernel
 cudaError_t launch_gemv_ws_int4(const GemvArgs& a, bool bf16, cudaStream_t st);
+cudaError_t launch_gemv_ws_nf4(const GemvArgs& a, bool bf16, cudaStream_t st);
 cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st);
 
 // ------------------------------------------------------ tensor-core GEMM
