@@ -217,9 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = n < p.N;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
-    // per-group constants, with the next group's raw values fetched early
-    uint32_t s_raw = 0, z_raw = 0, s_nxt = 0, z_nxt = 0;
-    float am = 0.f, am_nxt = 0.f;
+    // per-group constants, with the raw values of the next two groups (NF4:
+    // 64-row blocks) in flight, so a global load has two groups' worth of
+    // MMAs to land
+    uint32_t s_raw = 0, z_raw = 0, s_nxt = 0, z_nxt = 0, s_nx2 = 0, z_nx2 = 0;
+    float am = 0.f, am_nxt = 0.f, am_nx2 = 0.f;
     auto fetch = [&](int kb, uint32_t& s_out, uint32_t& z_out, float& am_out) {  // kb: absolute K block
       if (!ok || kb >= kb0 + nkb || FMT == kFmtInt4Act) return;
       if (FMT == kFmtInt4) {
@@ -230,8 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         am_out = p.absmax[(size_t)kb * p.N + n];  // 64-row blocks == stages
       }
     };
+    constexpr int kStep = FMT == kFmtNF4 ? 1 : 2;  // K blocks per group
     fetch(kb0, s_raw, z_raw, am);
-    fetch(kb0 + (FMT == kFmtNF4 ? 1 : 2), s_nxt, z_nxt, am_nxt);
+    fetch(kb0 + kStep, s_nxt, z_nxt, am_nxt);
+    fetch(kb0 + 2 * kStep, s_nx2, z_nx2, am_nx2);
     uint32_t zmix = dq_zmix_f16(z_raw), s2 = s_raw * 0x10001u;
     DqConstBF16 cbf = dq_const_bf16(z_raw, s_raw);
 
@@ -243,7 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_raw = s_nxt;
         z_raw = z_nxt;
         am = am_nxt;
-        fetch(kb0 + (FMT == kFmtNF4 ? it + 1 : it + 2), s_nxt, z_nxt, am_nxt);
+        s_nxt = s_nx2;
+        z_nxt = z_nx2;
+        am_nxt = am_nx2;
+        fetch(kb0 + it + 2 * kStep, s_nx2, z_nx2, am_nx2);
         if (FMT == kFmtInt4) {
           if (BF16) cbf = dq_const_bf16(z_raw, s_raw);
           else {

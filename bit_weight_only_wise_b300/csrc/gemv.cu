@@ -1,37 +1,30 @@
-// Split-K weight-streaming kernel for decode shapes (1 <= M <= 16).
+// Split-K weight-streaming kernel for act-order decode shapes (1 <= M <= 16,
+// g_idx as stored: every K row may belong to a different group).  Plain groups
+// and NF4 run on the warp-specialized kernel (gemv_ws.cu); this one serves the
+// stored act-order layout, where each packed word needs the (scale, zero) of
+// eight different groups, gathered from global memory per row.  For speed,
+// prepack act-order checkpoints once (act_order.cu) and use the plain kernels.
 //
-// Y[M,N] = X[M,K] . W_hat[K,N].  At M <= 16 the product moves 0.5 byte of
-// packed weight per multiply-add pair per token, so the kernel is bound by
-// HBM bandwidth: decode time is the time to stream the weights once
-// ("LLM量化技术深度对比:GPTQ vs AWQ vs bitsandbytes 2026基准全解析", key-data
-// item 3: 16 GB of 4-bit weights vs 64 GB at FP16 per forward; item 1: the
-// fused kernel that never writes 16-bit weights is the fast one).
+// Y[M,N] = X[M,K] . W_hat[K,N] ("GPTQ与bitsandbytes对比：谁是2024年大模型量化的终极选择？",
+// GPTQ section, --act-order).
 //
 // Work split (stream-K).  The work is cut into units of 256 output columns x
 // one 128-row K group (16 KB of packed weights).  A persistent grid of
-// 148 x (2 to 4) CTAs takes contiguous, equal-sized ranges of the units in
+// 148 x (2 to 3) CTAs takes contiguous, equal-sized ranges of the units in
 // column-block-major order, so every SM streams the same number of bytes
 // whatever the shape.  Inside a CTA each of the 8 warps owns a 32-column slice
-// of the unit and runs its own TMA ring: lane 0 keeps 2-3 2-KB tiles
+// of the unit and runs its own TMA ring: lane 0 keeps 2 2-KB tiles
 // (16 word-rows x 32 columns, 128-byte swizzle) in flight into the warp's
-// shared-memory stages, signalled by per-stage mbarriers; no registers are
-// spent on prefetching and no CTA-wide synchronisation is needed.
+// shared-memory stages, signalled by per-stage mbarriers.
 //
 // Inner product.  Lane (g = lane/4, c = lane%4) reads, per unit, four 16-byte
 // vectors (columns [4g, 4g+4) of word-rows 2c, 2c+8, 2c+1, 2c+9 -- an order
 // that makes the swizzled reads bank-conflict free), dequantizes them in
 // registers to exact fp16/bf16 pairs and feeds them to m16n8k16 tensor-core
 // MMAs as the A operand, the output columns being the MMA's M dimension and
-// the (up to 16) tokens its N dimension (fp32 accumulation).  The MMA only
-// needs the same K order in A and B: each lane's pair j = rows (j, j+4) of a
-// word meets the activations of the same two rows.
+// the (up to 16) tokens its N dimension (fp32 accumulation).
 //
-// Reduction.  A column block covered by one CTA is written directly.  A block
-// shared by several CTAs (at most the first and last block of each range) is
-// reduced through the workspace: each contributor writes its fp32 partial
-// slice and takes a ticket; the last one sums the partials in contributor
-// order -- deterministic whatever the arrival order -- rounds once, and resets
-// the ticket for the next call.
+// Reduction: the deterministic split-K write-out of gemv_common.cuh.
 #include <cuda.h>
 
 #include "dq_common.cuh"
@@ -75,62 +68,6 @@ template <int FMT, bool BF16>
 struct Dq;
 
 template <bool BF16>
-struct Dq<kInt4, BF16> {
-  // Lane L of the warp owns column L of the 32-column slice: it fetches that
-  // column's scale and zero one unit ahead, turns them into the three packed
-  // constants and publishes them in the warp's shared-memory table; each lane
-  // then reads the constants of its four columns with three 16-byte loads.
-  uint32_t* tab;  // [2 buffers][3][32] words, per warp
-  uint32_t s_nxt, z_nxt;
-  DqConstF16 cf[4];
-  DqConstBF16 cb[4];
-  int buf = 0;
-  __device__ __forceinline__ void fetch(const GemvArgs& a, int g, int slice0, int lane) {
-    const int n = slice0 + lane;
-    if (n < a.N) {
-      s_nxt = __ldg(a.scales + (size_t)g * a.N + n);
-      z_nxt = (__ldg(a.qz + (size_t)g * (a.N >> 3) + (n >> 3)) >> (4 * (n & 7))) & 0xFu;
-    } else {
-      s_nxt = z_nxt = 0;
-    }
-  }
-  // publish the fetched constants (call before the warp's __syncwarp), ...
-  __device__ __forceinline__ void publish(int lane) {
-    uint32_t* t = tab + buf * 96;
-    if (BF16) {
-      const DqConstBF16 k = dq_const_bf16(z_nxt, s_nxt);
-      t[lane] = k.z;
-      t[32 + lane] = k.s_hi;
-      t[64 + lane] = k.s_lo;
-    } else {
-      const DqConstF16 k = dq_const_f16(z_nxt, s_nxt);
-      t[lane] = k.z_lo;
-      t[32 + lane] = k.z_hi;
-      t[64 + lane] = k.s;
-    }
-  }
-  // ... and read this lane's four columns (after it)
-  __device__ __forceinline__ void begin(int gl) {
-    const uint32_t* t = tab + buf * 96;
-    const uint4 v0 = *reinterpret_cast<const uint4*>(t + 4 * gl);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(t + 32 + 4 * gl);
-    const uint4 v2 = *reinterpret_cast<const uint4*>(t + 64 + 4 * gl);
-    const uint32_t a0[4] = {v0.x, v0.y, v0.z, v0.w}, a1[4] = {v1.x, v1.y, v1.z, v1.w},
-                   a2[4] = {v2.x, v2.y, v2.z, v2.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (BF16) cb[c] = DqConstBF16{a0[c], a1[c], a2[c]};
-      else cf[c] = DqConstF16{a0[c], a1[c], a2[c]};
-    }
-    buf ^= 1;
-  }
-  __device__ __forceinline__ void word(const GemvArgs&, int, uint32_t w, int c4, int, int, bool, uint32_t out[4]) {
-    if (BF16) dq_word_bf16(w, cb[c4], out);
-    else dq_word_f16(w, cf[c4], out);
-  }
-};
-
-template <bool BF16>
 struct Dq<kInt4Act, BF16> {
   uint32_t* tab;
   __device__ __forceinline__ void fetch(const GemvArgs&, int, int, int) {}
@@ -171,36 +108,6 @@ struct Dq<kInt4Act, BF16> {
   }
 };
 
-template <bool BF16>
-struct Dq<kNF4, BF16> {
-  uint32_t* tab;
-  const float* cbk;  // shared-memory codebook
-  float4 am_nxt[2];  // absmax of the unit's two 64-row blocks, one unit ahead
-  float4 am[2];
-  int gl4;           // first of this lane's four columns, within the slice
-  __device__ __forceinline__ void fetch(const GemvArgs& a, int g, int slice0, int) {
-    const int col0 = slice0 + gl4;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int blk = 2 * g + h;
-      am_nxt[h] = (col0 < a.N && 64 * blk < a.K)
-                      ? __ldg(reinterpret_cast<const float4*>(a.absmax + (size_t)blk * a.N + col0))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  __device__ __forceinline__ void publish(int) {}
-  __device__ __forceinline__ void begin(int) {
-    am[0] = am_nxt[0];
-    am[1] = am_nxt[1];
-  }
-  __device__ __forceinline__ void word(const GemvArgs&, int o, uint32_t w, int c4, int, int, bool,
-                                       uint32_t out[4]) {
-    const float4 v = am[o & 1];  // tile rows 0..7 lie in block 0, rows 8..15 in block 1
-    const float amc = c4 == 0 ? v.x : c4 == 1 ? v.y : c4 == 2 ? v.z : v.w;
-    dq_word_nf4<BF16>(w, cbk, amc, out);
-  }
-};
-
 template <int NT, int FMT, bool BF16>
 __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 16, FMT))
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const GemvArgs a) {
@@ -208,7 +115,6 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   constexpr int kStage = stage_bytes<NT>();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kWarps][kRing];
-  __shared__ float s_cb[16];
   __shared__ __align__(16) uint32_t s_tab[kWarps][2 * 96];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -227,12 +133,6 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
 
   Dq<FMT, BF16> dq;
   dq.tab = s_tab[warp];
-  if constexpr (FMT == kNF4) {
-    dq.gl4 = 4 * gl;
-    if (threadIdx.x < 16) s_cb[threadIdx.x] = a.codebook[threadIdx.x];
-    __syncthreads();
-    dq.cbk = s_cb;
-  }
   if (lane == 0) {
     for (int s = 0; s < kRing; ++s) mbar_init(&bar[s], 1);
     fence_mbar_init();
