@@ -190,7 +190,7 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
       const uint32_t zw = *reinterpret_cast<const uint32_t*>(st + L::ZR + 4 * lane);
       const uint32_t sb[8] = {sv.x, sv.x >> 16, sv.y, sv.y >> 16, sv.z, sv.z >> 16, sv.w, sv.w >> 16};
       uint32_t k0[8], k1[8], k2[8];
-  #pragma unroll
+#pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t z = (zw >> (4 * j)) & 0xFu;
         if (BF16) {
