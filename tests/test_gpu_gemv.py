@@ -186,3 +186,66 @@ def test_act_order_entry_out_of_range_is_reported(M):
             dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
+
+
+def _assert_rows_exact(got, want, dtype):
+    # bit for bit, except that a weight of -0 comes out of the product as +0
+    # (the exact sum -0 + 0*w + ... is +0 in IEEE arithmetic)
+    gv, wv = numerics.dtype_bits_to_f64(got, dtype), numerics.dtype_bits_to_f64(want, dtype)
+    bad = np.nonzero((got != want) & ~((gv == 0) & (wv == 0)))
+    assert bad[0].size == 0, f"{bad[0].size} mismatches, first at {bad[0][0]},{bad[1][0]}"
+
+
+def _exhaustive_scale_checkpoint(dtype):
+    # every code q (0..15) x every zero point (0..15) x every positive finite
+    # fp16 scale and a spread of negative ones, in one 128-row group.  For
+    # fp16 outputs the scales stop where 15 * s would overflow: an infinite
+    # weight times a zero activation in another row would turn the whole
+    # column's sum into NaN.
+    top = 0x7C00 if dtype == "bf16" else 0x6C43  # 4366 * 15 < 65504
+    s_bits = np.concatenate([np.arange(1, top, dtype=np.uint16),
+                             (np.arange(1, top, 61, dtype=np.uint16) | 0x8000)]).astype(np.uint16)
+    N = 16 * s_bits.size
+    N += (-N) % 8
+    K = 128
+    q = np.tile((np.arange(K) % 16).astype(np.uint8)[:, None], (1, N))
+    z = (np.arange(N) % 16).astype(np.uint8)[None, :]
+    sc = np.resize(np.repeat(s_bits, 16), N).view(np.float16)[None, :]
+    return q, sc, z
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M", [16, 64])
+def test_fused_dequant_exact_over_every_scale(dtype, M):
+    # one-hot activation rows pick weight rows out of the product, so the
+    # decode kernel (M=16) and the tensor-core kernel (M=64) must reproduce
+    # RNE((q - z) * s) bit for bit on every code, zero point and fp16 scale
+    q, sc, z = _exhaustive_scale_checkpoint(dtype)
+    K, N = q.shape
+    rows = np.arange(M) % K
+    X = torch.zeros((M, K), dtype=TDT[dtype])
+    X[torch.arange(M), torch.from_numpy(rows)] = 1.0
+    Y = w4.gemm(X.cuda(), to_dev_u32(int4.pack_along_k(q)), to_dev(sc), to_dev_u32(int4.pack_zeros(z)))
+    want = int4.dequant(q, sc, z, dtype)[rows]
+    _assert_rows_exact(bits(Y), want, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M", [16, 64])
+def test_fused_nf4_dequant_exact_over_wide_absmax(dtype, M):
+    # NF4 through the fused kernels, one-hot rows: RNE(fl32(C[q] * absmax))
+    # bit for bit for every code and absmax values over many binades
+    K = 128
+    rng = np.random.default_rng(5)
+    cb = nf4.codebook()
+    N = 8192
+    hi = 40 if dtype == "bf16" else 15  # fp16: keep every weight finite (see above)
+    am = (2.0 ** rng.uniform(-40, hi, size=(K // 64, N))).astype(np.float32)
+    codes = np.tile((np.arange(K) % 16).astype(np.uint8)[:, None], (1, N))
+    codes = (codes + np.arange(N)[None, :]) % 16
+    rows = np.arange(M) % K
+    X = torch.zeros((M, K), dtype=TDT[dtype])
+    X[torch.arange(M), torch.from_numpy(rows)] = 1.0
+    Y = w4.nf4_gemm(X.cuda(), to_dev_u32(int4.pack_along_k(codes.astype(np.uint8))), to_dev(am), to_dev(cb))
+    want = nf4.nf4_dequant(codes.astype(np.uint8), am, cb, dtype)[rows]
+    _assert_rows_exact(bits(Y), want, dtype)
