@@ -189,26 +189,39 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
     if (col[h] < a.N) a.Y[col[h]] = (uint16_t)(pack2_rn(sum[h], 0.f, BF16) & 0xFFFFu);
 }
 
+// Ticket increment with acquire semantics that wraps to 0 once it reaches
+// `wrap` (atom.inc): the contributor that completes the count finds
+// old == wrap, and the ticket is back at zero for the next call without a
+// separate store (whose completion a fence would have to wait for).
+__device__ __forceinline__ uint32_t ticket_inc_acquire(int* p, uint32_t wrap) {
+  uint32_t old;
+  asm volatile("atom.acquire.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(wrap) : "memory");
+  return old;
+}
+
 // The CTA is done: publish this warp's partials of split blocks p0 and p1
 // (the CTA's first and last block; -1 for none) and take their tickets; the
-// contributor that completes a block's count sums it and resets the ticket.
+// contributor that completes a block's count sums it.
 template <int NT, bool BF16>
 __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R, int warp, int lane, int p0, int p1) {
   if (p0 < 0 && p1 < 0) return;
   // the warp barrier orders every lane's partial stores before lane 0's
-  // fence, whose release covers them before the tickets move
+  // fence, whose release covers them before the tickets move; the acquire
+  // increments order the summing loads after the other contributors' stores
   __syncwarp();
   int last0 = 0, last1 = 0;
   if (lane == 0) {
     __threadfence();
-    int* t0 = a.counters + p0 * kSliceWarps + warp;
-    int* t1 = a.counters + p1 * kSliceWarps + warp;
-    if (p0 >= 0) last0 = atomicAdd(t0, 1) == R.owner((long long)(p0 + 1) * a.G - 1) - R.owner((long long)p0 * a.G);
-    if (p1 >= 0) last1 = atomicAdd(t1, 1) == R.owner((long long)(p1 + 1) * a.G - 1) - R.owner((long long)p1 * a.G);
-    if (last0) *t0 = 0;  // ready for the next call
-    if (last1) *t1 = 0;
-    if (last0 || last1) __threadfence();
+    if (p0 >= 0) {
+      const uint32_t w = (uint32_t)(R.owner((long long)(p0 + 1) * a.G - 1) - R.owner((long long)p0 * a.G));
+      last0 = ticket_inc_acquire(a.counters + p0 * kSliceWarps + warp, w) == w;
+    }
+    if (p1 >= 0) {
+      const uint32_t w = (uint32_t)(R.owner((long long)(p1 + 1) * a.G - 1) - R.owner((long long)p1 * a.G));
+      last1 = ticket_inc_acquire(a.counters + p1 * kSliceWarps + warp, w) == w;
+    }
   }
+  __syncwarp();
   last0 = __shfl_sync(0xFFFFFFFFu, last0, 0);
   last1 = __shfl_sync(0xFFFFFFFFu, last1, 0);
   if (last0 && last1 && a.M == 1) {  // both blocks: one round trip for the two
