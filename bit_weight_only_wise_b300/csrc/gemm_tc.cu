@@ -341,13 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");  // the dequant warps only
       if (dw == 0 && lane == 0) {
-        __threadfence();
-        const int last = atomicAdd(p.counters + tile, 1) == p.splits - 1;
-        if (last) {
-          p.counters[tile] = 0;  // ready for the next call
-          __threadfence();
-        }
-        bars->last = last;
+        __threadfence();  // release: this CTA's tile is in memory before its ticket moves
+        bars->last = ticket_inc_acquire(p.counters + tile, (uint32_t)(p.splits - 1)) == (uint32_t)(p.splits - 1);
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
       if (bars->last && ok) {
@@ -356,12 +351,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           float acc[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-          for (int z = 0; z < p.splits; ++z) {
-            float v[8];
+          // four splits' loads in flight per round trip, summed in split order
+          for (int z0 = 0; z0 < p.splits; z0 += 4) {
+            float v[4][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __ldcg(base + (size_t)z * tile_floats + (size_t)(c + j) * kBN + nl);
+            for (int zz = 0; zz < 4; ++zz)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] += v[j];
+              for (int j = 0; j < 8; ++j)
+                v[zz][j] = z0 + zz < p.splits
+                               ? __ldcg(base + (size_t)(z0 + zz) * tile_floats + (size_t)(c + j) * kBN + nl)
+                               : 0.f;
+#pragma unroll
+            for (int zz = 0; zz < 4; ++zz)
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (z0 + zz < p.splits) acc[j] += v[zz][j];
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {

@@ -13,6 +13,7 @@
 #include <cstdint>
 
 #include "dq_common.cuh"
+#include "sm100.cuh"
 #include "w4a16_internal.h"
 
 namespace w4a16 {
@@ -189,16 +190,6 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
     if (col[h] < a.N) a.Y[col[h]] = (uint16_t)(pack2_rn(sum[h], 0.f, BF16) & 0xFFFFu);
 }
 
-// Ticket increment with acquire semantics that wraps to 0 once it reaches
-// `wrap` (atom.inc): the contributor that completes the count finds
-// old == wrap, and the ticket is back at zero for the next call without a
-// separate store (whose completion a fence would have to wait for).
-__device__ __forceinline__ uint32_t ticket_inc_acquire(int* p, uint32_t wrap) {
-  uint32_t old;
-  asm volatile("atom.acquire.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(wrap) : "memory");
-  return old;
-}
-
 // The CTA is done: publish this warp's partials of split blocks p0 and p1
 // (the CTA's first and last block; -1 for none) and take their tickets; the
 // contributor that completes a block's count sums it.
@@ -214,11 +205,11 @@ __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R,
     __threadfence();
     if (p0 >= 0) {
       const uint32_t w = (uint32_t)(R.owner((long long)(p0 + 1) * a.G - 1) - R.owner((long long)p0 * a.G));
-      last0 = ticket_inc_acquire(a.counters + p0 * kSliceWarps + warp, w) == w;
+      last0 = sm100::ticket_inc_acquire(a.counters + p0 * kSliceWarps + warp, w) == w;
     }
     if (p1 >= 0) {
       const uint32_t w = (uint32_t)(R.owner((long long)(p1 + 1) * a.G - 1) - R.owner((long long)p1 * a.G));
-      last1 = ticket_inc_acquire(a.counters + p1 * kSliceWarps + warp, w) == w;
+      last1 = sm100::ticket_inc_acquire(a.counters + p1 * kSliceWarps + warp, w) == w;
     }
   }
   __syncwarp();

@@ -23,6 +23,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Split-K ticket: an increment with acquire semantics that wraps to 0 once it
+// reaches `wrap` (atom.inc).  The contributor that completes the count finds
+// old == wrap, and the ticket is back at zero for the next call without a
+// separate store (whose completion a fence would have to wait for).
+__device__ __forceinline__ uint32_t ticket_inc_acquire(int* p, uint32_t wrap) {
+  uint32_t old;
+  asm volatile("atom.acquire.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(wrap) : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
