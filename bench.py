@@ -448,6 +448,21 @@ def run_gpu(args):
         for i in range(4):
             w4.gemm(xp[i], *layer[i], out=yp[i])
 
+    # gate_up timed alone first (the GPU idle before it): the burst peak applies
+    torch.cuda.synchronize()
+    time.sleep(0.5)
+    gate_layer = stack[0][2]
+    for _ in range(2):
+        w4.gemm(xp[2], *gate_layer, out=yp[2])
+    torch.cuda.synchronize()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(cur)
+    for _ in range(3):
+        w4.gemm(xp[2], *gate_layer, out=yp[2])
+    b1.record(cur)
+    torch.cuda.synchronize()
+    gate_burst = 2 * M_PREFILL * 5120 * 55296 / (b0.elapsed_time(b1) / 3 * 1e-3) / 1e12
+
     pre_steps = max(3, min(args.steps, 20))
     pre_ms = timed(prefill_step, pre_steps, max(args.warmup, 3), cur)
     tflops = world * LAYER_FLOPS * pre_steps / (pre_ms * 1e-3) / 1e12
@@ -517,10 +532,18 @@ def run_gpu(args):
             "unit": "TFLOP/s",
             "ms_per_step": round(pre_ms / pre_steps, 3),
             "per_linear_ms": {n: round(t, 4) for (n, _, _), t in zip(LINEARS, lin_ms)},
-            "roofline": {"bound": "tensor", "achieved": round(gate, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                         "frac": round(gate / tc_peak, 4), "peak_source": peak_src,
-                         "frac_of_sustained": round(gate / tc_sustained, 4) if tc_sustained else None,
-                         "kernel": "gemm_tc_kernel on gate_up 5120x55296"},
+            # gate_up timed right after the long prefill loop: a kernel inside a
+            # long step, so the sustained (power-capped) peak is the denominator
+            "roofline": {"bound": "tensor", "achieved": round(gate, 1),
+                         "peak": tc_sustained if tc_sustained else tc_peak, "unit": "TFLOP/s",
+                         "peak_kind": "sustained" if tc_sustained else "burst",
+                         "frac": round(gate / (tc_sustained if tc_sustained else tc_peak), 4),
+                         "frac_of_burst": round(gate / tc_peak, 4), "peak_source": peak_src,
+                         "kernel": "gemm_tc_kernel on gate_up 5120x55296, inside the prefill loop"},
+            "burst": {"achieved": round(gate_burst, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                      "frac": round(gate_burst / tc_peak, 4),
+                      "how": "gate_up 5120x55296 at M=4096 timed alone (3 calls after an idle pause), "
+                             "before the prefill loop"},
             "layer_frac_of_peak": round(tflops / world / tc_peak, 4),
         },
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

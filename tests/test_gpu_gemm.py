@@ -190,3 +190,35 @@ def test_gemm_split_k_is_deterministic_and_matches():
     cols = sample_columns(N)
     Y_ref, A = int4_expected(W, X.cpu().double().numpy()[rows], "bf16", cols)
     assert_close(to_f64(Y1)[np.ix_(rows, cols)], Y_ref, A, "split-K 5120x5120 M=256")
+
+
+def test_tickets_are_left_at_zero():
+    # the split-K tickets wrap back to zero at each block's contributor count:
+    # after decode calls (split column blocks on every shape below) and a
+    # split-K prefill call through one workspace, the ticket area is all zero
+    ticket_bytes = 4096 * 8 * 4  # one int per 32-column slice of up to 4096 column blocks
+    shapes = [(1, 5120, 5120), (5, 27648, 1024), (16, 2048, 3072), (256, 5120, 1280)]
+    need = max(w4.workspace_bytes(M, N, K) for M, K, N in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev())
+    st = _status()
+    for M, K, N in shapes:
+        W = gaussian_weights(K, N, 0.02, M + N)
+        qw, sc, qz = w4.quantize(to_dev(W))
+        X = activations(M, K, "bf16", M).cuda()
+        for _ in range(3):
+            w4.gemm(X, qw, sc, qz, ws=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert torch.count_nonzero(ws[:ticket_bytes]).item() == 0, f"tickets left set after M={M} {K}x{N}"
+    # the act-order decode kernel (g_idx as stored) takes the same tickets
+    from synth import act_order_g_idx
+
+    K, N = 4096, 1024
+    g_idx = act_order_g_idx(K, 128, 3)
+    W = student_t_weights(K, N, 5, 0.01, 3)
+    (qw, sc, qz, gi), _ = _int4_dev(W, g_idx)
+    for M in (1, 9):
+        w4.gemm(activations(M, K, "f16", M).cuda(), qw, sc, qz, g_idx=gi, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.count_nonzero(ws[:ticket_bytes]).item() == 0, "tickets left set after act-order decode"
