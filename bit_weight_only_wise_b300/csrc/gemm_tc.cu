@@ -9,18 +9,20 @@
 // X^T is the B operand, staged in shared memory by TMA with 128-byte swizzle
 // (K-major).  The fp32 accumulator D[128 x BT] also lives in TMEM.
 //
-// Pipeline (one CTA, 10 warps):
+// Pipeline (one CTA, 18 warps):
 //   warp 0     TMA producer: per 64-row K block, the X tile [BT x 64] and the
 //              packed weight tile [8 word-rows x 128 columns] into a ring of
 //              shared-memory stages (mbarrier with transaction count).
 //   warp 1     allocates TMEM; one lane issues the MMAs (4 x K=16 per stage)
 //              and commits them to mbarriers that free the stage and the A
 //              buffer.
-//   warps 2-9  dequantize: thread = one output column (its TMEM lane), each of
-//              the two warps sharing a lane quarter takes 4 of the stage's 8
-//              word-rows; codes -> exact fp16/bf16 pairs in natural K order ->
-//              tcgen05.st into one of 4 A buffers.  After the K loop the same
-//              warps read D back (tcgen05.ld) and write Y.
+//   warps 2-17 dequantize, in two groups of 8 that take alternate K blocks
+//              (so two blocks' loads, arithmetic and TMEM stores overlap):
+//              thread = one output column (its TMEM lane), each of the two
+//              warps of a group sharing a lane quarter takes 4 of the stage's
+//              8 word-rows; codes -> exact fp16/bf16 pairs in natural K order
+//              -> tcgen05.st into one of 4 A buffers.  After the K loop the
+//              16 warps read D back (tcgen05.ld) and write Y.
 //
 // Dequantization follows the pages' format (cloud.tencent.com/developer/
 // article/2726413 §2.1-2.2: asymmetric, one scale and zero point per group of
@@ -48,12 +50,16 @@ constexpr int kBK = 64;        // K rows per stage
 constexpr int kMaxBT = 256;    // tokens per CTA (MMA N)
 constexpr int kStages = 4;
 constexpr int kABufs = 4;
-#ifndef W4A16_GEMM_DQ_WARPS
-#define W4A16_GEMM_DQ_WARPS 16
-#endif
-constexpr int kDqWarps = W4A16_GEMM_DQ_WARPS;     // 8 or 16 dequantizing warps
+constexpr int kDqWarps = 16;                      // dequantizing warps
 constexpr int kParts = kDqWarps / 4;              // warps sharing one TMEM lane quarter
-constexpr int kWords = (kBK / 8) / kParts;        // packed words per thread per stage
+// The dequantizing warps form two groups that take alternate K blocks, so two
+// blocks are in flight: one group's loads, arithmetic and TMEM stores overlap
+// the other's.
+constexpr int kDqGroups = 2;
+constexpr int kGroupWarps = kDqWarps / kDqGroups;
+constexpr int kWords = (kBK / 8) / (kGroupWarps / 4);  // packed words per thread per stage
+static_assert(kWords == 4 && kStages % kDqGroups == 0 && kABufs % kDqGroups == 0,
+              "each group keeps to its own stages and A buffers");
 constexpr int kThreads = 32 * (2 + kDqWarps);
 constexpr int kWStageBytes = (kBK / 8) * kBN * 4;  // 4 KB
 constexpr uint32_t kTmemCols = 512;
@@ -134,10 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], kDqWarps + 1);
+      mbar_init(&bars->empty[s], kGroupWarps + 1);
     }
     for (int b = 0; b < kABufs; ++b) {
-      mbar_init(&bars->a_full[b], kDqWarps);
+      mbar_init(&bars->a_full[b], kGroupWarps);
       mbar_init(&bars->a_empty[b], 1);
     }
     mbar_init(&bars->d_full, 1);
@@ -210,15 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------- dequant + epilogue
     const int dw = warp - 2;
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-    const int h = dw >> 2;         // which kWords word-rows of a stage
+    const int quarter = warp & 3;              // TMEM lane quarter this warp may access
+    const int grp = dw / kGroupWarps;          // K blocks grp, grp + 2, ...
+    const int h = (dw % kGroupWarps) >> 2;     // which kWords word-rows of a stage
+    const int ep = dw >> 2;                    // epilogue: which quarter of the tokens
     const int nl = quarter * 32 + lane;
     const int n = n0 + nl;
     const bool ok = n < p.N;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
-    // per-group constants, with the raw values of the next two groups (NF4:
-    // 64-row blocks) in flight, so a global load has two groups' worth of
+    // the current K block's constants, with the raw values of this group's
+    // next two blocks in flight, so a global load has four blocks' worth of
     // MMAs to land
     uint32_t s_raw = 0, z_raw = 0, s_nxt = 0, z_nxt = 0, s_nx2 = 0, z_nx2 = 0;
     float am = 0.f, am_nxt = 0.f, am_nx2 = 0.f;
@@ -232,18 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         am_out = p.absmax[(size_t)kb * p.N + n];  // 64-row blocks == stages
       }
     };
-    constexpr int kStep = FMT == kFmtNF4 ? 1 : 2;  // K blocks per group
-    fetch(kb0, s_raw, z_raw, am);
-    fetch(kb0 + kStep, s_nxt, z_nxt, am_nxt);
-    fetch(kb0 + 2 * kStep, s_nx2, z_nx2, am_nx2);
+    // this group's K blocks are kb0 + grp + 2i: one 128-row INT4 group (kb0 is
+    // group aligned), or one 64-row NF4 block, apart
+    constexpr int kStep = kDqGroups;
+    fetch(kb0 + grp, s_raw, z_raw, am);
+    fetch(kb0 + grp + kStep, s_nxt, z_nxt, am_nxt);
+    fetch(kb0 + grp + 2 * kStep, s_nx2, z_nx2, am_nx2);
     uint32_t zmix = dq_zmix_f16(z_raw), s2 = s_raw * 0x10001u;
     DqConstBF16 cbf = dq_const_bf16(z_raw, s_raw);
 
     bool alive = true;
-    for (int it = 0; it < nkb && alive; ++it) {
+    for (int it = grp; it < nkb && alive; it += kDqGroups) {
       const int s = it % kStages;
       const int b = it % kABufs;
-      if (it > 0 && (FMT == kFmtNF4 || (it & 1) == 0)) {
+      if (it > grp) {
         s_raw = s_nxt;
         z_raw = z_nxt;
         am = am_nxt;
@@ -310,8 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         alive = false;
         break;
       }
-      if constexpr (kWords == 4) tmem_st_x16(tmem + lane_off + kTmemA + 32u * b + 16u * h, regs);
-      else tmem_st_x8(tmem + lane_off + kTmemA + 32u * b + 8u * h, regs);
+      tmem_st_x16(tmem + lane_off + kTmemA + 32u * b + 16u * h, regs);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = (int)(blockIdx.x + gridDim.x * blockIdx.y);
       const size_t tile_floats = (size_t)p.BT * kBN;
       float* mine = p.partial + ((size_t)tile * p.splits + blockIdx.z) * tile_floats;
-      for (int c = h * part; c < (h + 1) * part; c += 8) {
+      for (int c = ep * part; c < (ep + 1) * part; c += 8) {
         uint32_t v[8];
         tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
         tmem_wait_ld();
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
       if (bars->last && ok) {
         const float* base = p.partial + (size_t)tile * p.splits * tile_floats;
-        for (int c = h * part; c < (h + 1) * part; c += 8) {
+        for (int c = ep * part; c < (ep + 1) * part; c += 8) {
           float acc[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) acc[j] = 0.f;
@@ -376,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (done && !*abort) {
       const int part = p.BT / kParts;  // tokens per warp, a multiple of 8
-      for (int c = h * part; c < (h + 1) * part; c += 8) {
+      for (int c = ep * part; c < (ep + 1) * part; c += 8) {
         uint32_t v[8];
         tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
         tmem_wait_ld();
