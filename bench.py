@@ -33,6 +33,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -72,13 +73,14 @@ _REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_pow
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons during a timed region."""
 
-    def __init__(self, index=0):
+    def __init__(self, index=0, path=None):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # the raw samples: a kept file when a path is given, else a temporary one
+        self.path = path or os.path.join(tempfile.gettempdir(), f"w4a16_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
         q = "clocks.sm,clocks.max.sm,power.draw," + ",".join("clocks_event_reasons." + r for r in _REASONS)
         try:
             self.proc = subprocess.Popen(
@@ -409,7 +411,7 @@ def run_gpu(args):
         return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
     cur = torch.cuda.current_stream(dev)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clock_log) as clk:
         dec_ms = timed(g.replay, args.steps, args.warmup, cur)
     clocks = clk.summary()
     dec_step_ms = dec_ms / args.steps
@@ -569,6 +571,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-config timing sweep")
+    ap.add_argument("--clock-log", default=None, help="keep the raw nvidia-smi clock samples in this CSV file")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
