@@ -279,7 +279,7 @@ const char* w4a16_status_string(w4a16_status status) {
   switch (status) {
     case W4A16_OK: return "ok";
     case W4A16_ERR_INVALID_ARG: return "invalid argument (shape, pointer, alignment, dtype or workspace)";
-    case W4A16_ERR_UNSUPPORTED: return "unsupported by this build (group or block size, or shape)";
+    case W4A16_ERR_UNSUPPORTED: return "not supported by this library (group or block size, or shape)";
     case W4A16_ERR_CUDA: return "CUDA runtime or launch error";
     case W4A16_ERR_TIMEOUT: return "device-side bounded wait expired";
   }

@@ -64,7 +64,7 @@ extern "C" {
 typedef enum {
   W4A16_OK = 0,
   W4A16_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, bad dtype */
-  W4A16_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  W4A16_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
   W4A16_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   W4A16_ERR_TIMEOUT = 4      /* a device-side bounded wait expired (written to dev_status) */
 } w4a16_status;
