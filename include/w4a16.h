@@ -83,9 +83,10 @@ typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
  *   workspace: device scratch of at least w4a16_workspace_bytes(M, N, K)
  *     bytes, zero-filled by the caller before its first use.  Its first part
  *     holds the split-K tickets, which every call that completes leaves at
- *     zero again; the rest is scratch for fp32 partial sums.  May be NULL when
- *     that size is 0.  Calls that run at the same time must not share a
- *     workspace.
+ *     zero again; the rest is scratch for fp32 partial sums.  After a call
+ *     whose status word reports W4A16_ERR_TIMEOUT, zero-fill it again.  May
+ *     be NULL when that size is 0.  Calls that run at the same time must not
+ *     share a workspace.
  *   dev_status: NULL, or a device int the caller zeroes; a kernel whose
  *     bounded wait expires writes W4A16_ERR_TIMEOUT there and stops early
  *     (its Y is then undefined); a g_idx entry outside [0, K/128) writes
