@@ -27,6 +27,7 @@
 // outside the arrays.
 #include <cstdint>
 
+#include "sm100.cuh"
 #include "w4a16_internal.h"
 
 namespace w4a16 {
@@ -77,9 +78,15 @@ __global__ void __launch_bounds__(256)
   out[(size_t)i * N + n] = w;
 }
 
+// Launched as a programmatic dependent of the previous kernel in the stream
+// and letting the next one (the product) launch at once, so that the
+// product's launch overlaps this one; X, perm and the scratch it writes are
+// touched only after the previous kernel has completed.
 __global__ void __launch_bounds__(256)
     gather_columns_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ perm, int M, int K,
                           uint16_t* __restrict__ out) {
+  sm100::griddep_launch_dependents();
+  sm100::griddep_wait();
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= K) return;
   int src = perm[j];
@@ -100,8 +107,16 @@ cudaError_t launch_act_order_prepack(const uint32_t* qw, const int32_t* g_idx, i
 
 cudaError_t launch_gather_columns(const uint16_t* X, const int32_t* perm, int M, int K, uint16_t* out,
                                   cudaStream_t st) {
-  gather_columns_kernel<<<dim3((K + 255) / 256, M < 65535 ? M : 65535), 256, 0, st>>>(X, perm, M, K, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((K + 255) / 256, M < 65535 ? M : 65535);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_columns_kernel, X, perm, M, K, out);
 }
 
 }  // namespace w4a16

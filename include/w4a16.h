@@ -48,6 +48,14 @@
  *  - Pointers must be 16-byte aligned.  N and K must be multiples of 8;
  *    K a multiple of the group / block size.
  *  - M == 0 or N == 0 is a valid empty problem: W4A16_OK, nothing launched.
+ *  - The product kernels are launched as programmatic dependents of the
+ *    kernel before them on `stream`: they start copying qweight, scales,
+ *    qzeros, absmax and the codebook while that kernel may still be running,
+ *    and touch X, g_idx / perm, Y and the workspace only after it has
+ *    completed.  A kernel that writes the weights directly before a call
+ *    must therefore not signal early completion
+ *    (cudaTriggerProgrammaticLaunchCompletion) before those writes; an
+ *    ordinary kernel, a copy or an event between the two needs nothing.
  *  - The dtype of X and Y is `dtype`; scales are always fp16, absmax fp32.
  */
 #ifndef W4A16_H
