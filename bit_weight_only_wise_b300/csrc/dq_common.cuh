@@ -209,6 +209,53 @@ __device__ __forceinline__ void dq_word_bf16_rows(uint32_t w, const DqConstBF16 
   out[3] = dq_pair_bf16(lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u), c[3]);
 }
 
+// ------------------------------------------ INT4, bf16 through fp32 FMAs
+// The same bf16 value from the fp16 route's magic codes and one
+// mixed-precision FMA per weight (fp16 operands, exact product, fp32 sum):
+//     fma(1024 + q, s, -(1024 + z) * s) = (q - z) * s   exactly,
+// because -(1024 + z) * s has at most 22 significant bits (an exact fp32
+// constant) and the result at most 15; likewise with 64 + q for the codes in
+// bits 4..7.  One cvt.rn.bf16x2 then rounds each value of a pair once.  The
+// FMAs issue on the fp32 pipe at full rate, leaving the packed 16-bit pipe
+// idle: per pair 2 FMAs, 1 conversion and 1.25 logic operations, against 3
+// packed operations and 1.75 logic operations above.  Only the sign of a
+// zero weight can differ from the IEEE product (x + (-x) is +0); a product
+// cannot show it, since its fp32 sums start from +0.
+struct DqConstBF16Fma {
+  float z_lo;  // -(1024 + z) * s: pairs 0 and 2
+  float z_hi;  // -(64 + z) * s: pairs 1 and 3
+  uint32_t s;  // fp16 scale in the low half
+};
+
+__device__ __forceinline__ DqConstBF16Fma dq_const_bf16_fma(uint32_t z, uint32_t s_bits) {
+  const float s = __half2float(__ushort_as_half((unsigned short)(s_bits & 0xFFFFu)));
+  DqConstBF16Fma c;
+  c.z_lo = __fmul_rn(-(1024.f + (float)z), s);  // exact
+  c.z_hi = __fmul_rn(-(64.f + (float)z), s);    // exact
+  c.s = s_bits & 0xFFFFu;
+  return c;
+}
+
+__device__ __forceinline__ uint32_t dq_pair_bf16_fma(uint32_t p, float zs, uint32_t s) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 a0, a1, s0, s1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\t"
+      "mov.b32 {s0, s1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, a0, s0, %4;\n\t"
+      "fma.rn.f32.f16 %1, a1, s0, %4;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(p), "r"(s), "f"(zs));
+  return pack2_rn(lo, hi, true);
+}
+
+__device__ __forceinline__ void dq_word_bf16_fma(uint32_t w, const DqConstBF16Fma& c, uint32_t out[4]) {
+  const uint32_t w8 = w >> 8;
+  out[0] = dq_pair_bf16_fma(lop3_and_or(w, 0x000F000Fu, 0x64006400u), c.z_lo, c.s);
+  out[1] = dq_pair_bf16_fma(lop3_and_or(w, 0x00F000F0u, 0x54005400u), c.z_hi, c.s);
+  out[2] = dq_pair_bf16_fma(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), c.z_lo, c.s);
+  out[3] = dq_pair_bf16_fma(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), c.z_hi, c.s);
+}
+
 // -------------------------------------------------- natural K order pairs
 // The tensor-memory A operand needs each 32-bit cell to hold two consecutive
 // K rows, (2j, 2j+1).  Byte j of a word holds exactly those two codes; a byte

@@ -5,9 +5,10 @@
 // ("LLM量化技术深度对比:GPTQ vs AWQ vs bitsandbytes 2026基准全解析", key-data
 // item 3: a 4-bit forward moves a quarter of the FP16 bytes; item 1: the fused
 // kernel that never writes 16-bit weights is the fast one).  What keeps such
-// a kernel from the bandwidth is instruction issue: exact bf16 dequantization
-// costs three packed 16-bit operations per pair of weights, so every other
-// instruction per weight has to go.  The CTA is therefore split by role:
+// a kernel from the bandwidth is instruction issue: exact dequantization costs
+// two packed 16-bit operations per pair of weights (fp16) or two fp32 FMAs and
+// a conversion (bf16), so every other instruction per weight has to go.  The
+// CTA is therefore split by role:
 //
 //   producer warp  streams each unit (256 columns x one 128-row group) into a
 //                  shared-memory stage: eight 2-KB weight boxes (16 word-rows
@@ -194,10 +195,10 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
       for (int j = 0; j < 8; ++j) {
         const uint32_t z = (zw >> (4 * j)) & 0xFu;
         if (BF16) {
-          const DqConstBF16 q = dq_const_bf16(z, sb[j] & 0xFFFFu);
-          k0[j] = q.z;
-          k1[j] = q.s_hi;
-          k2[j] = q.s_lo;
+          const DqConstBF16Fma q = dq_const_bf16_fma(z, sb[j] & 0xFFFFu);
+          k0[j] = __float_as_uint(q.z_lo);
+          k1[j] = __float_as_uint(q.z_hi);
+          k2[j] = q.s;
         } else {
           const DqConstF16 q = dq_const_f16(z, sb[j] & 0xFFFFu);
           k0[j] = q.z_lo;
@@ -317,8 +318,11 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
             dq_word_nf4<BF16>(wd[2 * rr], cbk, __uint_as_float(am[2 * rr]), pa);
             dq_word_nf4<BF16>(wd[2 * rr + 1], cbk, __uint_as_float(am[2 * rr + 1]), pb);
           } else if (BF16) {
-            dq_word_bf16(wd[2 * rr], DqConstBF16{k0[2 * rr], k1[2 * rr], k2[2 * rr]}, pa);
-            dq_word_bf16(wd[2 * rr + 1], DqConstBF16{k0[2 * rr + 1], k1[2 * rr + 1], k2[2 * rr + 1]}, pb);
+            dq_word_bf16_fma(wd[2 * rr], DqConstBF16Fma{__uint_as_float(k0[2 * rr]), __uint_as_float(k1[2 * rr]), k2[2 * rr]},
+                             pa);
+            dq_word_bf16_fma(wd[2 * rr + 1],
+                             DqConstBF16Fma{__uint_as_float(k0[2 * rr + 1]), __uint_as_float(k1[2 * rr + 1]), k2[2 * rr + 1]},
+                             pb);
           } else {
             dq_word_f16(wd[2 * rr], DqConstF16{k0[2 * rr], k1[2 * rr], k2[2 * rr]}, pa);
             dq_word_f16(wd[2 * rr + 1], DqConstF16{k0[2 * rr + 1], k1[2 * rr + 1], k2[2 * rr + 1]}, pb);
