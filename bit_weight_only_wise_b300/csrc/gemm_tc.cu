@@ -415,12 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int FMT, bool BF16>
 cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const GemmParams& p, dim3 grid,
                       cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<unsigned long long> attr_done{0};
+  unsigned long long dev_bit = 0;
+  if (attrs_pending(attr_done, &dev_bit)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMaxSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_done.fetch_or(dev_bit, std::memory_order_release);
   }
   const int smem = smem_fixed<FMT>() + (FMT == kFmtInt4Act ? (p.K / 128) * kActTableRowBytes : 0);
   if (smem > kMaxSmem) return cudaErrorInvalidValue;

@@ -307,8 +307,9 @@ cudaError_t launch_one(const CUtensorMap& tm, const GemvArgs& a, cudaStream_t st
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<unsigned long long> attr_done{0};
+  unsigned long long dev_bit = 0;
+  if (attrs_pending(attr_done, &dev_bit)) {
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          gemv_smem<NT>());
     if (e != cudaSuccess) return e;
@@ -317,7 +318,7 @@ cudaError_t launch_one(const CUtensorMap& tm, const GemvArgs& a, cudaStream_t st
     e = cudaFuncSetAttribute(gemv_kernel<NT, FMT, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr_done.fetch_or(dev_bit, std::memory_order_release);
   }
   // programmatic dependent launch: this grid may start while the previous
   // kernel on the stream finishes (it waits for it before touching its data)

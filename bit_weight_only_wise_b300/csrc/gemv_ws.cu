@@ -400,15 +400,16 @@ cudaError_t launch_ws(const CUtensorMap& tmW, const CUtensorMap& tmA, const Gemv
   if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.X, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 128,
                  (uint32_t)(8 * NT), CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<unsigned long long> attr_done{0};
+  unsigned long long dev_bit = 0;
+  if (attrs_pending(attr_done, &dev_bit)) {
     cudaError_t e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr_done.fetch_or(dev_bit, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.ctas);

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime_api.h>
@@ -89,6 +90,18 @@ GemmSplit gemm_split_plan(int M, int N, int K, bool act_order);
 // Whether the act-order variant's per-CTA (scale, zero) table fits for this K.
 bool gemm_act_order_fits(int K);
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st);
+
+// ------------------------------------------------- per-device kernel setup
+// cudaFuncSetAttribute acts on a kernel as loaded on the current device, so a
+// launcher sets its kernel's attributes once per device: `done` keeps one bit
+// per device index.  Returns whether they still have to be set here; *bit is
+// the bit to record afterwards (0 past device 63: those set them every call).
+inline bool attrs_pending(const std::atomic<unsigned long long>& done, unsigned long long* bit) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  *bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  return *bit == 0 || (done.load(std::memory_order_acquire) & *bit) == 0;
+}
 
 // ------------------------------------------------------ act-order prepack
 cudaError_t launch_act_order_prepack(const uint32_t* qw, const int32_t* g_idx, int K, int N, int group_size,
