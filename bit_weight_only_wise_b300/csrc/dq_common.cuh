@@ -18,6 +18,9 @@
 //         s_hi the first 8 significant bits of s (exact in bf16) and s_lo the
 //         remaining <= 3 bits (also exact); t = (q - z) * s_lo is exact (<= 7
 //         bits) and fma(q - z, s_hi, t) rounds the exact (q - z) * s once.
+//   bf16 through fp32 (the decode kernel): the fp16 magic codes go through
+//         one mixed-precision FMA each, which gives (q - z) * s exactly in
+//         fp32, and one pair conversion rounds it (see below).
 //
 // A packed word holds the codes of 8 consecutive K rows of one column; pair j
 // (j = 0..3) of a word holds rows (j, j + 4) in its (low, high) halves.
