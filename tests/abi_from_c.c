@@ -1,0 +1,77 @@
+/*
+ * The library used through include/w4a16.h from a plain C program, with no
+ * GPU: every entry point the header declares is referenced (so the link
+ * checks that each has C linkage), and the calls made are the pure host
+ * functions and calls that fail validation before anything is launched.
+ * Prints "ok" and exits 0 when every check holds; otherwise prints the first
+ * failing check and exits 1.  Built and run by tests/test_c_abi_host.py.
+ */
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "w4a16.h"
+
+#define CHECK(c)                                          \
+  do {                                                    \
+    if (!(c)) {                                           \
+      printf("failed: %s (line %d)\n", #c, __LINE__);     \
+      return 1;                                           \
+    }                                                     \
+  } while (0)
+
+/* stand-ins for device pointers: 16-byte aligned, never dereferenced,
+   because every call below is rejected (or is an empty problem) first */
+#define P(a) ((void*)(uintptr_t)(a))
+#define PU(a) ((uint32_t*)(uintptr_t)(a))
+#define PF(a) ((float*)(uintptr_t)(a))
+
+int main(void) {
+  typedef void (*fn_t)(void);
+  const fn_t fns[] = {
+      (fn_t)w4a16_gemm,          (fn_t)w4a16_gemv,
+      (fn_t)nf4_gemm,            (fn_t)w4a16_dequant,
+      (fn_t)nf4_dequant,         (fn_t)w4a16_quantize,
+      (fn_t)nf4_quantize,        (fn_t)w4a16_gemv_noalloc,
+      (fn_t)w4a16_workspace_bytes, (fn_t)w4a16_act_order_prepack,
+      (fn_t)w4a16_gemm_prepacked, (fn_t)w4a16_prepacked_workspace_bytes,
+      (fn_t)w4a16_selftest_wait_timeout, (fn_t)w4a16_status_string,
+  };
+  for (size_t i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i) CHECK(fns[i] != NULL);
+
+  for (int s = W4A16_OK; s <= W4A16_ERR_TIMEOUT; ++s) {
+    const char* msg = w4a16_status_string((w4a16_status)s);
+    CHECK(msg != NULL && strlen(msg) >= 2);
+  }
+
+  /* pure host functions */
+  CHECK(w4a16_workspace_bytes(0, 4096, 4096) == 0);
+  CHECK(w4a16_workspace_bytes(1, 4096, 4096) == w4a16_workspace_bytes(1, 4096, 4096));
+  CHECK(w4a16_prepacked_workspace_bytes(4, 64, 256) >= (size_t)4 * 256 * 2);
+
+  /* validation: rejected before any launch */
+  CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, 64, 256, 128, (w4a16_dtype)7, NULL, 0, NULL,
+                   NULL) == W4A16_ERR_INVALID_ARG);
+  CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, 60, 256, 128, W4A16_BF16, NULL, 0, NULL, NULL) ==
+        W4A16_ERR_INVALID_ARG);
+  CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, 64, 256, 64, W4A16_BF16, NULL, 0, NULL, NULL) ==
+        W4A16_ERR_UNSUPPORTED);
+  CHECK(w4a16_gemm(NULL, PU(16), P(16), PU(16), NULL, P(16), 4, 64, 256, 128, W4A16_F16, NULL, 0, NULL, NULL) ==
+        W4A16_ERR_INVALID_ARG);
+  CHECK(w4a16_gemv(P(16), PU(16), P(16), PU(16), NULL, P(16), 17, 64, 256, 128, W4A16_BF16, NULL, 0, NULL, NULL) ==
+        W4A16_ERR_INVALID_ARG);
+  CHECK(w4a16_gemv_noalloc(P(16), PU(16), P(16), PU(16), NULL, P(16), 17, 64, 256, 128, W4A16_BF16, NULL, NULL) ==
+        W4A16_ERR_INVALID_ARG);
+  CHECK(nf4_gemm(P(16), PU(16), PF(16), PF(16), P(16), 4, 64, 256, 32, W4A16_BF16, NULL, 0, NULL, NULL) ==
+        W4A16_ERR_UNSUPPORTED);
+  CHECK(w4a16_selftest_wait_timeout(NULL, 1000, NULL) == W4A16_ERR_INVALID_ARG);
+
+  /* empty problems: valid no-ops that launch nothing and touch no pointer */
+  CHECK(w4a16_gemm(NULL, PU(16), P(16), PU(16), NULL, NULL, 0, 64, 256, 128, W4A16_BF16, NULL, 0, NULL, NULL) ==
+        W4A16_OK);
+  CHECK(w4a16_gemv_noalloc(NULL, PU(16), P(16), PU(16), NULL, NULL, 0, 64, 256, 128, W4A16_BF16, NULL, NULL) ==
+        W4A16_OK);
+
+  printf("ok\n");
+  return 0;
+}
