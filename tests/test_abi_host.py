@@ -106,3 +106,14 @@ def test_workspace_sizes_are_pure_and_bounded(lib):
             b = lib.w4a16_workspace_bytes(M, N, K)
             assert b == lib.w4a16_workspace_bytes(M, N, K)
             assert b <= 64 * 1024 * 1024
+
+
+def test_noalloc_scratch_fits_every_decode_call(lib):
+    # the header promises that the allocation-free decode entry's fixed
+    # scratch array serves every M <= 16 under the current split-K plan
+    m = re.search(r"#define\s+W4A16_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", open(HEADER).read())
+    assert m, "W4A16_NOALLOC_SCRATCH_BYTES not found"
+    scratch = int(m.group(1)) << int(m.group(2))
+    for M in range(1, 17):
+        for K, N in ((128, 8), (4096, 4096), (5120, 55296), (4095 * 128, 256), (256, 4096 * 256)):
+            assert lib.w4a16_workspace_bytes(M, N, K) <= scratch, (M, N, K)
