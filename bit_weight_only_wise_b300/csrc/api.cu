@@ -16,7 +16,13 @@ namespace {
 
 constexpr int kInt4Group = 128;
 constexpr int kNF4Block = 64;
-constexpr int kMaxK = 65535 * 8;  // word-rows index a grid dimension
+static_assert(W4A16_MAX_K == 65535 * 8, "word-rows index a grid dimension");
+static_assert(W4A16_MAX_N == kMaxColBlocks * kGemvCols, "one split-K ticket slice per column block");
+// token tiles of the tensor-core kernel (up to 128 tokens with act-order)
+// index a grid dimension; tiles = column tiles x token tiles then fits int
+static_assert(W4A16_MAX_M == 65535 * 128, "token tiles index a grid dimension");
+
+bool in_limits(int M, int N, int K) { return M <= W4A16_MAX_M && N <= W4A16_MAX_N && K <= W4A16_MAX_K; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
@@ -27,16 +33,16 @@ w4a16_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A
 
 // Shape checks common to the INT4 entry points.  Returns OK, or the error.
 w4a16_status check_int4_shape(int M, int N, int K, int group_size) {
-  if (M < 0 || N < 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
-  if (N % 8 || K % 8 || K > kMaxK || N > kMaxColBlocks * kGemvCols) return W4A16_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K <= 0 || !in_limits(M, N, K)) return W4A16_ERR_INVALID_ARG;
+  if (N % 8 || K % 8) return W4A16_ERR_INVALID_ARG;
   if (group_size <= 0 || K % group_size) return W4A16_ERR_INVALID_ARG;
   if (group_size != kInt4Group) return W4A16_ERR_UNSUPPORTED;
   return W4A16_OK;
 }
 
 w4a16_status check_nf4_shape(int M, int N, int K, int blocksize) {
-  if (M < 0 || N < 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
-  if (N % 8 || K % 8 || K > kMaxK || N > kMaxColBlocks * kGemvCols) return W4A16_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K <= 0 || !in_limits(M, N, K)) return W4A16_ERR_INVALID_ARG;
+  if (N % 8 || K % 8) return W4A16_ERR_INVALID_ARG;
   if (blocksize <= 0 || K % blocksize) return W4A16_ERR_INVALID_ARG;
   if (blocksize != kNF4Block) return W4A16_ERR_UNSUPPORTED;
   return W4A16_OK;
@@ -222,7 +228,7 @@ w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const flo
 }
 
 size_t w4a16_workspace_bytes(int M, int N, int K) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || !in_limits(M, N, K)) return 0;
   if (M <= W4A16_GEMV_MAX_M) return gemv_plan(M, N, K, kInt4).workspace_bytes;
   // the tensor-core kernel's split-K tiles; act-order uses a smaller token tile
   const size_t a = gemm_split_plan(M, N, K, false).workspace_bytes;
@@ -251,7 +257,7 @@ static size_t prepacked_front_bytes(int M, int N, int K) {
 }
 
 size_t w4a16_prepacked_workspace_bytes(int M, int N, int K) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || !in_limits(M, N, K)) return 0;
   return prepacked_front_bytes(M, N, K) + align256((size_t)M * K * 2);
 }
 

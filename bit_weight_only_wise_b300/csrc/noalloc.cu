@@ -56,7 +56,8 @@ extern "C" w4a16_status w4a16_gemv_noalloc(const void* X, const uint32_t* qweigh
                                            const uint32_t* qzeros, const int32_t* g_idx, void* Y, int M, int N,
                                            int K, int group_size, w4a16_dtype dtype, int* dev_status,
                                            cudaStream_t stream) {
-  if (M < 0 || M > W4A16_GEMV_MAX_M || N < 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+  if (M < 0 || M > W4A16_GEMV_MAX_M || N < 0 || N > W4A16_MAX_N || K <= 0 || K > W4A16_MAX_K)
+    return W4A16_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return W4A16_OK;
   const size_t need = w4a16_workspace_bytes(M, N, K);
   if (need > (size_t)W4A16_NOALLOC_SCRATCH_BYTES) return W4A16_ERR_UNSUPPORTED;

@@ -47,6 +47,9 @@
  *    at the caller's next synchronisation, as for any CUDA call.
  *  - Pointers must be 16-byte aligned.  N and K must be multiples of 8;
  *    K a multiple of the group / block size.
+ *  - Sizes: 0 <= M <= W4A16_MAX_M, 0 <= N <= W4A16_MAX_N and
+ *    0 < K <= W4A16_MAX_K; outside them W4A16_ERR_INVALID_ARG, nothing
+ *    launched.
  *  - M == 0 or N == 0 is a valid empty problem: W4A16_OK, nothing launched.
  *  - The product kernels are launched as programmatic dependents of the
  *    kernel before them on `stream`: they start copying qweight, scales,
@@ -81,6 +84,14 @@ typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
 
 /* Largest token count the split-K decode kernel (w4a16_gemv) accepts. */
 #define W4A16_GEMV_MAX_M 16
+
+/* Size limits of every entry point.  M: 65535 token tiles of 128 (a grid
+ * dimension); N: 4096 column blocks of 256 (the split-K ticket area); K:
+ * 65535 packed word-rows of 8 (a grid dimension), so the largest K that is a
+ * multiple of 128 is 524160. */
+#define W4A16_MAX_M 8388480
+#define W4A16_MAX_N 1048576
+#define W4A16_MAX_K 524280
 
 /*
  * Y = X . W_hat for the INT4 format, any M >= 0.  Dispatches on M: M <= 16
@@ -183,7 +194,8 @@ w4a16_status w4a16_gemv_noalloc(const void* X, const uint32_t* qweight, const vo
                                 int group_size, w4a16_dtype dtype, int* dev_status, cudaStream_t stream);
 
 /* Bytes of workspace w4a16_gemm / w4a16_gemv / nf4_gemm need for this
- * shape (0 when none is needed).  Pure host function. */
+ * shape (0 when none is needed, and for shapes outside the size limits,
+ * which those calls reject).  Pure host function. */
 size_t w4a16_workspace_bytes(int M, int N, int K);
 
 /*
@@ -224,7 +236,8 @@ w4a16_status w4a16_gemm_prepacked(const void* X, const uint32_t* qweight_sorted,
                                   int K, int group_size, w4a16_dtype dtype, void* workspace,
                                   size_t workspace_bytes, int* dev_status, cudaStream_t stream);
 
-/* Bytes of workspace w4a16_gemm_prepacked needs.  Pure host function. */
+/* Bytes of workspace w4a16_gemm_prepacked needs (0 for shapes outside the
+ * size limits).  Pure host function. */
 size_t w4a16_prepacked_workspace_bytes(int M, int N, int K);
 
 /*

@@ -66,6 +66,14 @@ int main(void) {
         W4A16_ERR_UNSUPPORTED);
   CHECK(w4a16_selftest_wait_timeout(NULL, 1000, NULL) == W4A16_ERR_INVALID_ARG);
 
+  /* size limits */
+  CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), W4A16_MAX_M + 1, 64, 256, 128, W4A16_BF16, NULL, 0,
+                   NULL, NULL) == W4A16_ERR_INVALID_ARG);
+  CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, W4A16_MAX_N + 8, 256, 128, W4A16_BF16, NULL, 0,
+                   NULL, NULL) == W4A16_ERR_INVALID_ARG);
+  CHECK(w4a16_workspace_bytes(W4A16_MAX_M + 1, 64, 256) == 0);
+  CHECK(w4a16_prepacked_workspace_bytes(4, W4A16_MAX_N + 8, 256) == 0);
+
   /* empty problems: valid no-ops that launch nothing and touch no pointer */
   CHECK(w4a16_gemm(NULL, PU(16), P(16), PU(16), NULL, NULL, 0, 64, 256, 128, W4A16_BF16, NULL, 0, NULL, NULL) ==
         W4A16_OK);

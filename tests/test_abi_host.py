@@ -117,3 +117,34 @@ def test_noalloc_scratch_fits_every_decode_call(lib):
     for M in range(1, 17):
         for K, N in ((128, 8), (4096, 4096), (5120, 55296), (4095 * 128, 256), (256, 4096 * 256)):
             assert lib.w4a16_workspace_bytes(M, N, K) <= scratch, (M, N, K)
+
+
+def _header_int(name):
+    m = re.search(rf"#define\s+{name}\s+(\d+)", open(HEADER).read())
+    assert m, name
+    return int(m.group(1))
+
+
+def test_size_limits(lib):
+    # sizes past the header's limits are rejected before anything is launched,
+    # and the pure size functions do no arithmetic on them
+    import bit_weight_only_wise_b300 as w4
+
+    MAX_M, MAX_N, MAX_K = (_header_int(n) for n in ("W4A16_MAX_M", "W4A16_MAX_N", "W4A16_MAX_K"))
+    assert (MAX_M, MAX_N, MAX_K) == (65535 * 128, 4096 * 256, 65535 * 8)
+    INV = w4.ERR_INVALID_ARG
+    assert _gemm(lib, M=MAX_M + 1) == INV
+    assert _gemm(lib, M=2**31 - 1) == INV
+    assert _gemm(lib, N=MAX_N + 8) == INV
+    assert _gemm(lib, K=(MAX_K // 128 + 1) * 128) == INV
+    assert lib.nf4_gemm(16, 16, 16, 16, 16, MAX_M + 1, 64, 256, 64, 1, None, 0, None, None) == INV
+    assert lib.w4a16_gemv_noalloc(16, 16, 16, 16, None, 16, 1, 2**31 - 8, 256, 128, 1, None, None) == INV
+    assert lib.w4a16_gemv_noalloc(16, 16, 16, 16, None, 16, 1, 64, 2**31 - 8, 128, 1, None, None) == INV
+    big = 2**31 - 1
+    for M, N, K in ((big, 64, 256), (4, big, 256), (4, 64, big), (big, big, big), (MAX_M + 1, MAX_N, MAX_K)):
+        assert lib.w4a16_workspace_bytes(M, N, K) == 0, (M, N, K)
+        assert lib.w4a16_prepacked_workspace_bytes(M, N, K) == 0, (M, N, K)
+    # at the limits themselves the sizes are defined and bounded
+    for M in (1, 16, 17, 4096, MAX_M):
+        for N, K in ((MAX_N, 128), (256, MAX_K // 128 * 128), (MAX_N, MAX_K // 128 * 128)):
+            assert 0 <= lib.w4a16_workspace_bytes(M, N, K) <= 1 << 36, (M, N, K)
