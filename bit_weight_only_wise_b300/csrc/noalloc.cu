@@ -17,6 +17,7 @@
 // workspace.  All calls share the one array, so calls that overlap on the GPU
 // (different streams, no ordering between them) race on it and must not be
 // issued.
+#include <cstdint>
 #include <mutex>
 
 #include "w4a16.h"
@@ -56,9 +57,18 @@ extern "C" w4a16_status w4a16_gemv_noalloc(const void* X, const uint32_t* qweigh
                                            const uint32_t* qzeros, const int32_t* g_idx, void* Y, int M, int N,
                                            int K, int group_size, w4a16_dtype dtype, int* dev_status,
                                            cudaStream_t stream) {
-  if (M < 0 || M > W4A16_GEMV_MAX_M || N < 0 || N > W4A16_MAX_N || K <= 0 || K > W4A16_MAX_K)
+  // every check of w4a16_gemv, in its order, before the scratch or the stream
+  // is touched: a rejected call has no side effect
+  if (dtype != W4A16_F16 && dtype != W4A16_BF16) return W4A16_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K <= 0 || M > W4A16_MAX_M || N > W4A16_MAX_N || K > W4A16_MAX_K)
     return W4A16_ERR_INVALID_ARG;
+  if (N % 8 || K % 8 || group_size <= 0 || K % group_size) return W4A16_ERR_INVALID_ARG;
+  if (group_size != 128) return W4A16_ERR_UNSUPPORTED;
+  if (M > W4A16_GEMV_MAX_M) return W4A16_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return W4A16_OK;
+  auto ok16 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!ok16(X) || !ok16(qweight) || !ok16(scales) || !ok16(qzeros) || !ok16(Y)) return W4A16_ERR_INVALID_ARG;
+  if (g_idx && (reinterpret_cast<uintptr_t>(g_idx) & 15u)) return W4A16_ERR_INVALID_ARG;
   const size_t need = w4a16_workspace_bytes(M, N, K);
   if (need > (size_t)W4A16_NOALLOC_SCRATCH_BYTES) return W4A16_ERR_UNSUPPORTED;
   void* scratch = nullptr;

@@ -6,6 +6,7 @@
  * Prints "ok" and exits 0 when every check holds; otherwise prints the first
  * failing check and exits 1.  Built and run by tests/test_c_abi_host.py.
  */
+#include <limits.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -25,6 +26,58 @@
 #define P(a) ((void*)(uintptr_t)(a))
 #define PU(a) ((uint32_t*)(uintptr_t)(a))
 #define PF(a) ((float*)(uintptr_t)(a))
+#define PI(a) ((int32_t*)(uintptr_t)(a))
+
+static int defined_host_status(w4a16_status s) {
+  return s == W4A16_OK || s == W4A16_ERR_INVALID_ARG || s == W4A16_ERR_UNSUPPORTED;
+}
+
+/* Every entry point over extreme and boundary sizes, block sizes and both
+ * dtypes.  Each call passes NULL as its first pointer, which every entry
+ * point checks after the sizes and before anything else, so no call can
+ * launch; what runs is the size and shape arithmetic, which a sanitizer
+ * build checks for undefined behaviour. */
+static int fuzz_sizes(void) {
+  const int sizes[] = {INT_MIN, -8, -1, 0, 1, 8, 16, 17, 128, 256, 4096, 524160,
+                       W4A16_MAX_M, W4A16_MAX_M + 1, W4A16_MAX_N, W4A16_MAX_N + 8, W4A16_MAX_K,
+                       W4A16_MAX_K + 8, INT_MAX - 7, INT_MAX};
+  const int blocks[] = {INT_MIN, -1, 0, 64, 128, INT_MAX};
+  const w4a16_dtype dts[] = {W4A16_F16, W4A16_BF16};
+  const size_t ns = sizeof(sizes) / sizeof(sizes[0]), nb = sizeof(blocks) / sizeof(blocks[0]);
+  for (size_t a = 0; a < ns; ++a)
+    for (size_t b = 0; b < ns; ++b)
+      for (size_t c = 0; c < ns; ++c) {
+        const int M = sizes[a], N = sizes[b], K = sizes[c];
+        (void)w4a16_workspace_bytes(M, N, K);
+        (void)w4a16_prepacked_workspace_bytes(M, N, K);
+        for (size_t g = 0; g < nb; ++g)
+          for (int d = 0; d < 2; ++d) {
+            const int G = blocks[g];
+            const w4a16_dtype dt = dts[d];
+            w4a16_status s1, s2;
+            CHECK(defined_host_status(
+                w4a16_gemm(NULL, PU(16), P(16), PU(16), NULL, P(16), M, N, K, G, dt, NULL, 0, NULL, NULL)));
+            s1 = w4a16_gemv(NULL, PU(16), P(16), PU(16), NULL, P(16), M, N, K, G, dt, NULL, 0, NULL, NULL);
+            s2 = w4a16_gemv_noalloc(NULL, PU(16), P(16), PU(16), NULL, P(16), M, N, K, G, dt, NULL, NULL);
+            CHECK(defined_host_status(s1) && s1 == s2);
+            CHECK(defined_host_status(w4a16_gemm_prepacked(NULL, PU(16), P(16), PU(16), PI(16), P(16), M, N, K, G,
+                                                           dt, P(16), 1u << 20, NULL, NULL)));
+            CHECK(defined_host_status(
+                nf4_gemm(NULL, PU(16), PF(16), PF(16), P(16), M, N, K, G, dt, NULL, 0, NULL, NULL)));
+            if (a == 0) { /* the weight-only entry points take no M */
+              CHECK(defined_host_status(w4a16_dequant(NULL, P(16), PU(16), NULL, P(16), K, N, G, dt, NULL)));
+              CHECK(defined_host_status(nf4_dequant(NULL, PF(16), PF(16), P(16), K, N, G, dt, NULL)));
+              if (d == 0) {
+                CHECK(defined_host_status(w4a16_quantize(NULL, K, N, G, PU(16), P(16), PU(16), NULL)));
+                CHECK(defined_host_status(nf4_quantize(NULL, K, N, G, PF(16), PU(16), PF(16), NULL)));
+                CHECK(defined_host_status(w4a16_act_order_prepack(NULL, PI(16), K, N, G, PU(32), PI(48), NULL,
+                                                                  NULL)));
+              }
+            }
+          }
+      }
+  return 0;
+}
 
 int main(void) {
   typedef void (*fn_t)(void);
@@ -79,6 +132,8 @@ int main(void) {
         W4A16_OK);
   CHECK(w4a16_gemv_noalloc(NULL, PU(16), P(16), PU(16), NULL, NULL, 0, 64, 256, 128, W4A16_BF16, NULL, NULL) ==
         W4A16_OK);
+
+  if (fuzz_sizes()) return 1;
 
   printf("ok\n");
   return 0;
