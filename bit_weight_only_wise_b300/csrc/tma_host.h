@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace w4a16 {
@@ -16,15 +17,20 @@ typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_
                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Looked up once (an atomic, so threads making their first call together do
+// not race; a failed lookup is retried on the next call).
 inline PFN_encodeTiled tensor_map_encoder() {
-  static PFN_encodeTiled fn = nullptr;
+  static std::atomic<PFN_encodeTiled> cached{nullptr};
+  PFN_encodeTiled fn = cached.load(std::memory_order_acquire);
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
     void* ptr = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<PFN_encodeTiled>(ptr);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
