@@ -83,12 +83,15 @@ def status_string(status: int) -> str:
     return _lib.w4a16_status_string(status).decode()
 
 
+# Pointers and streams go to ctypes as plain ints (or None for NULL): the
+# c_void_p argtypes convert them, which costs less per call than building
+# c_void_p objects.
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(device) -> ctypes.c_void_p:
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def workspace_bytes(M: int, N: int, K: int) -> int:
