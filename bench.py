@@ -55,6 +55,9 @@ def int4_bytes(K, N):
 
 
 STACK_BYTES = LAYERS * sum(int4_bytes(K, N) for _, K, N in LINEARS)
+# the decode step's activations and outputs: X [1, K] read and Y [1, N]
+# written once per launch, 16-bit
+STACK_XY_BYTES = LAYERS * sum(2 * (K + N) for _, K, N in LINEARS)
 LAYER_FLOPS = sum(2 * M_PREFILL * K * N for _, K, N in LINEARS)
 
 
@@ -249,6 +252,19 @@ def sweep_weights(torch, w4, K, N, kind, seed, dev):
     return (qw, sc, qz), nbytes
 
 
+def sweep_entry(name, K, N, M, dt, us, nbytes, hbm_peak, tc_peak):
+    """One timed configuration: weight bytes (codes and their group metadata)
+    per second, the same with X read and Y written once (16-bit) included, and
+    the product's FLOP rate, each against its roofline."""
+    gbs = nbytes / us / 1e3
+    tf = 2 * M * N * K / us / 1e6
+    xy = 2 * M * (K + N)
+    return {"config": name, "K": K, "N": N, "M": M, "dtype": dt, "us": round(us, 2), "GBs": round(gbs, 1),
+            "GBs_incl_xy": round((nbytes + xy) / us / 1e3, 1), "TFLOPs": round(tf, 1),
+            "hbm_frac": round(gbs / hbm_peak, 4), "tc_frac": round(tf / tc_peak, 4),
+            "bound": "hbm" if M <= 16 else ("both" if M < 256 else "tensor")}
+
+
 def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
     out = []
     for ci, (name, K, N, Ms, dt, kind) in enumerate(SWEEP):
@@ -305,12 +321,7 @@ def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
             e1.record(cur)
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1e3 / (n_rep * reps)
-            gbs = nbytes / us / 1e3
-            tf = 2 * M * N * K / us / 1e6
-            ent = {"config": name, "K": K, "N": N, "M": M, "dtype": dt, "us": round(us, 2), "GBs": round(gbs, 1),
-                   "TFLOPs": round(tf, 1), "hbm_frac": round(gbs / hbm_peak, 4), "tc_frac": round(tf / tc_peak, 4),
-                   "bound": "hbm" if M <= 16 else ("both" if M < 256 else "tensor")}
-            out.append(ent)
+            out.append(sweep_entry(name, K, N, M, dt, us, nbytes, hbm_peak, tc_peak))
             del gr, X, Y
         del sets, w, runs
         torch.cuda.empty_cache()
@@ -520,6 +531,7 @@ def run_gpu(args):
         "roofline": {
             "bound": "hbm",
             "achieved": round(achieved, 1),
+            "achieved_incl_xy": round(achieved * (STACK_BYTES + STACK_XY_BYTES) / STACK_BYTES, 1),
             "peak": hbm_peak,
             "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4),

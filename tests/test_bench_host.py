@@ -82,3 +82,22 @@ def test_decode_source_hash_covers_the_kernel_sources():
     assert len(h) == 64
     for f in bench.DECODE_SOURCES:
         assert os.path.exists(os.path.join(ROOT, "bit_weight_only_wise_b300", "csrc", f))
+
+
+def test_sweep_entry_rates():
+    # 4096 x 4096 at M = 16: 8,716,288 weight bytes (codes, fp16 scales,
+    # 4-bit zeros) in 10 us, plus X (16 x 4096) read and Y (16 x 4096)
+    # written once at 2 bytes each
+    e = bench.sweep_entry("C1", 4096, 4096, 16, "f16", 10.0, 8_716_288, 8000.0, 2000.0)
+    assert e["GBs"] == round(8_716_288 / 10.0 / 1e3, 1) == 871.6
+    assert e["GBs_incl_xy"] == round((8_716_288 + 2 * 16 * 8192) / 10.0 / 1e3, 1)
+    assert e["TFLOPs"] == round(2 * 16 * 4096 * 4096 / 10.0 / 1e6, 1)
+    assert e["hbm_frac"] == round(871.6288 / 8000.0, 4)
+    assert e["bound"] == "hbm"
+    assert bench.sweep_entry("x", 4096, 4096, 64, "bf16", 1.0, 1, 1.0, 1.0)["bound"] == "both"
+    assert bench.sweep_entry("x", 4096, 4096, 4096, "bf16", 1.0, 1, 1.0, 1.0)["bound"] == "tensor"
+
+
+def test_stack_xy_bytes():
+    assert bench.STACK_XY_BYTES == 64 * 2 * ((5120 + 7168) + (5120 + 5120) + (5120 + 55296) + (27648 + 5120))
+    assert bench.STACK_XY_BYTES < bench.STACK_BYTES // 1000  # activations are < 0.1% of the stream at M = 1
