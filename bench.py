@@ -218,7 +218,7 @@ SWEEP = (
     ("C4 Qwen down", 27648, 5120, (1, 256, 1024, 4096), "bf16", "int4"),
     ("C5 NF4", 8192, 8192, (1, 64, 1024), "bf16", "nf4"),
 )
-L2_BYTES = 126 * 2**20
+L2_BYTES = 126 * 2**20  # used when the device does not report its L2 size
 
 
 def sweep_weights(torch, w4, K, N, kind, seed, dev):
@@ -267,9 +267,11 @@ def sweep_entry(name, K, N, M, dt, us, nbytes, hbm_peak, tc_peak):
 
 def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
     out = []
+    # weight copies rotated through: more than 4x the device's L2 (queried)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_BYTES
     for ci, (name, K, N, Ms, dt, kind) in enumerate(SWEEP):
         w, nbytes = sweep_weights(torch, w4, K, N, kind, 1000 + ci, dev)
-        copies = max(2, -(-4 * L2_BYTES // nbytes))
+        copies = max(2, -(-4 * l2 // nbytes))
         sets = [w] + [tuple(t.clone() for t in w) for _ in range(copies - 1)]
         cb = w4.nf4_codebook(dev) if kind == "nf4" else None
         tdt = torch.bfloat16 if dt == "bf16" else torch.float16
