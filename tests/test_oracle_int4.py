@@ -155,3 +155,44 @@ def test_g_idx_groups_have_group_size_rows():
     g = act_order_g_idx(4096, 128, 0)
     assert np.all(np.bincount(g) == 128)
     assert not np.array_equal(g, np.arange(4096) // 128)
+
+
+@pytest.mark.parametrize("gs", [32, 64, 1024])
+def test_other_group_sizes(gs):
+    # the quantizer and dequantizer take the group size as a parameter (a
+    # finer grouping, or one group per column when it equals K); the grid
+    # invariant, the half-step bound and exact recovery of an exact grid
+    # must hold at every size, with the statistics taken per group of gs rows
+    K, N = 1024, 48
+    W = student_t_weights(K, N, 5, 0.01, gs)
+    q, s, z = _quant(W, gs=gs)
+    assert s.shape == (K // gs, N) and z.shape == (K // gs, N)
+    w_hat = int4.dequant_exact(q, s, z, gs)
+    s_rows = s.astype(np.float64)[np.arange(K) // gs]
+    z_rows = z.astype(np.float64)[np.arange(K) // gs]
+    ratio = w_hat / s_rows
+    assert np.array_equal(ratio, np.round(ratio))
+    assert np.all(ratio >= -z_rows) and np.all(ratio <= 15 - z_rows)
+    err = np.abs(W.astype(np.float64) - w_hat)
+    interior = (q != 0) & (q != 15)
+    assert np.all(err[interior] <= s_rows[interior] / 2)
+    assert np.all(err <= (0.5 + 15 * 2.0 ** -11 * (1 + 2.0 ** -11)) * s_rows)
+    # each group's scale comes from that group's own range: the range of the
+    # first group of column 0 is 15 steps of its scale to within fp16 rounding
+    g0 = W[:gs, 0].astype(np.float64)
+    rng_ = max(g0.max(), 0.0) - min(g0.min(), 0.0)
+    assert abs(float(s[0, 0]) * 15 - rng_) <= 15 * float(s[0, 0]) * 2.0 ** -10
+    # exact grid, recovered unchanged
+    rng = np.random.default_rng(gs)
+    z0 = rng.integers(0, 16, size=(K // gs, N))
+    q0 = rng.integers(0, 16, size=(K, N))
+    q0[::gs] = 0
+    q0[1::gs] = 15
+    s0 = 2.0 ** -7
+    Wg = ((q0 - z0[np.arange(K) // gs]) * s0).astype(np.float32)
+    q1, s1, z1 = _quant(Wg, gs=gs)
+    assert np.all(s1.astype(np.float64) == s0)
+    assert np.array_equal(z1, z0.astype(np.uint8)) and np.array_equal(q1, q0.astype(np.uint8))
+    # a different group size on the same weights gives different statistics
+    q2, s2, _ = _quant(W, gs=128 if gs != 128 else 64)
+    assert s2.shape != s.shape
