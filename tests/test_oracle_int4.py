@@ -196,3 +196,54 @@ def test_other_group_sizes(gs):
     # a different group size on the same weights gives different statistics
     q2, s2, _ = _quant(W, gs=128 if gs != 128 else 64)
     assert s2.shape != s.shape
+
+
+def test_zero_point_uses_the_stored_fp16_scale():
+    # The stored format keeps s in fp16 and the zero point is z = round(-min/s)
+    # with that stored s (cloud.tencent.com/developer/article/2726413 §2.1: an
+    # asymmetric grid stores a scale and a zero point; the fp16 scale is the
+    # stored one).  This group is built so that the fp16 rounding of s decides
+    # z.  With u = 2^-7:
+    #   min w = -(5.5 + 5.5 * 2^-14) * u,  max w = (9.5 + 24.5 * 2^-14) * u,
+    #   (max - min) / 15 = u * (1 + 2^-13), which rounds to s = u in fp16,
+    #   -min / s = 5.5 + 5.5 * 2^-14 -> z = 6,
+    # while the unrounded scale would give -min / (u (1 + 2^-13)) = 5.4997...
+    # -> 5.  Codes, by hand: min -> rint(-5.5003) + 6 = 0; max -> rint(9.5015)
+    # + 6 = 16 -> 15; 0 -> 6; u -> 7.
+    u = 2.0 ** -7
+    mn = -(5.5 + 5.5 * 2.0 ** -14) * u
+    mx = (9.5 + 24.5 * 2.0 ** -14) * u
+    W = np.zeros((128, 8), dtype=np.float32)
+    W[0, :] = mn
+    W[1, :] = mx
+    W[2, :] = u
+    assert float(np.float32(mn)) == mn and float(np.float32(mx)) == mx  # exact in fp32
+    q, s, z = _quant(W)
+    assert np.all(s.astype(np.float64) == u)
+    assert np.all(z == 6)
+    assert np.all(q[0] == 0) and np.all(q[1] == 15) and np.all(q[2] == 7) and np.all(q[3:] == 6)
+    # the zero weight reconstructs exactly through the stored z
+    assert np.all(int4.dequant_exact(q, s, z)[3:] == 0.0)
+
+
+def test_range_always_contains_zero():
+    # An asymmetric grid with a stored zero point represents 0 exactly (same
+    # passage), so the range of a group is taken with 0 included.  All-positive
+    # group: w = k * u for k = 1..15 (and copies), u = 2^-7.  With 0 in range:
+    # s = 15u / 15 = u, z = 0, q = k.  (Without it, s would be 14u / 15 in fp16
+    # and the codes would not be k.)
+    u = 2.0 ** -7
+    k = (np.arange(128) % 15) + 1
+    W = np.repeat((k * u).astype(np.float32)[:, None], 8, axis=1)
+    q, s, z = _quant(W)
+    assert np.all(s.astype(np.float64) == u)
+    assert np.all(z == 0)
+    assert np.array_equal(q[:, 0], k.astype(np.uint8))
+    # all-negative group: w = -k * u -> s = u, z = 15, q = 15 - k
+    qn, sn, zn = _quant(-W)
+    assert np.all(sn.astype(np.float64) == u)
+    assert np.all(zn == 15)
+    assert np.array_equal(qn[:, 0], (15 - k).astype(np.uint8))
+    # and in both, the weights come back exactly
+    assert np.array_equal(int4.dequant_exact(q, s, z), W.astype(np.float64))
+    assert np.array_equal(int4.dequant_exact(qn, sn, zn), -W.astype(np.float64))
