@@ -12,7 +12,7 @@ Tensor conventions (all CUDA, contiguous):
   qzeros   [K/128, N/8] torch.int32
   g_idx    [K] torch.int32 or None
   absmax   [K/64, N] torch.float32 (NF4)
-  codebook [16] torch.float32 (NF4)
+  codebook [16] torch.float32 (NF4), or None for the library's built-in table
 """
 
 from __future__ import annotations
@@ -50,6 +50,7 @@ _SIGS = {
     "w4a16_prepacked_workspace_bytes": [_i, _i, _i],
     "w4a16_selftest_wait_timeout": [_vp, ctypes.c_ulonglong, _vp],
     "w4a16_status_string": [_i],
+    "nf4_default_codebook": [_vp],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -160,8 +161,8 @@ def gemv(X, qweight, scales, qzeros, g_idx=None, out=None, group_size=GROUP_SIZE
     return _int4_call("w4a16_gemv", X, qweight, scales, qzeros, g_idx, out, group_size, ws, dev_status)
 
 
-def nf4_gemm(X, qweight, absmax, codebook, out=None, blocksize=NF4_BLOCK, ws=None, dev_status=None):
-    """Y = X . W_hat (NF4), any M."""
+def nf4_gemm(X, qweight, absmax, codebook=None, out=None, blocksize=NF4_BLOCK, ws=None, dev_status=None):
+    """Y = X . W_hat (NF4), any M.  ``codebook`` None: the built-in table."""
     K = qweight.shape[0] * 8
     N = qweight.shape[1]
     _check_x(X, K)
@@ -233,7 +234,7 @@ def dequant(qweight, scales, qzeros, g_idx=None, dtype=torch.bfloat16, group_siz
     return W
 
 
-def nf4_dequant(qweight, absmax, codebook, dtype=torch.bfloat16, blocksize=NF4_BLOCK):
+def nf4_dequant(qweight, absmax, codebook=None, dtype=torch.bfloat16, blocksize=NF4_BLOCK):
     K, N = qweight.shape[0] * 8, qweight.shape[1]
     W = torch.empty((K, N), dtype=dtype, device=qweight.device)
     st = _lib.nf4_dequant(_ptr(qweight), _ptr(absmax), _ptr(codebook), _ptr(W), K, N, blocksize, _DTYPES[dtype],
@@ -256,7 +257,7 @@ def quantize(W, group_size=GROUP_SIZE):
     return qweight, scales, qzeros
 
 
-def nf4_quantize(W, codebook, blocksize=NF4_BLOCK):
+def nf4_quantize(W, codebook=None, blocksize=NF4_BLOCK):
     """NF4 quantization of fp32 CUDA ``W[K, N]`` -> (qweight, absmax)."""
     if W.dtype != torch.float32 or not W.is_cuda or not W.is_contiguous():
         raise ValueError("W must be a contiguous CUDA float32 tensor")
@@ -270,13 +271,9 @@ def nf4_quantize(W, codebook, blocksize=NF4_BLOCK):
 
 
 def nf4_codebook(device="cuda") -> torch.Tensor:
-    """The 16-entry NF4 table: 0, 7 negative and 8 positive standard-normal
-    quantiles of evenly spaced probabilities up to 1 - (1/30 + 1/32)/2,
-    normalised to [-1, 1] (computed here in float64, stored as float32)."""
-    delta = 1.0 - 0.5 * (1.0 / 30.0 + 1.0 / 32.0)
-    d = torch.tensor(delta, dtype=torch.float64)
-    top = torch.special.ndtri(d)
-    pos = torch.special.ndtri(d - (d - 0.5) * torch.arange(8, dtype=torch.float64) / 8) / top
-    neg = -torch.special.ndtri(d - (d - 0.5) * torch.arange(7, dtype=torch.float64) / 7) / top
-    vals = torch.sort(torch.cat([neg, torch.zeros(1, dtype=torch.float64), pos])).values
-    return vals.to(torch.float32).to(device)
+    """The library's built-in 16-entry NF4 table (``nf4_default_codebook``),
+    as a float32 tensor on ``device``: the table a ``None`` codebook stands
+    for in :func:`nf4_gemm`, :func:`nf4_dequant` and :func:`nf4_quantize`."""
+    buf = (ctypes.c_float * 16)()
+    _check(_lib.nf4_default_codebook(ctypes.addressof(buf)), "nf4_default_codebook")
+    return torch.tensor(list(buf), dtype=torch.float32).to(device)

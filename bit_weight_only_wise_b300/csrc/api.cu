@@ -155,8 +155,8 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
   w4a16_status st = check_nf4_shape(M, N, K, blocksize);
   if (st != W4A16_OK) return st;
   if (M == 0 || N == 0) return W4A16_OK;
-  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(codebook16) || !ok_ptr(Y))
-    return W4A16_ERR_INVALID_ARG;
+  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(Y)) return W4A16_ERR_INVALID_ARG;
+  if (codebook16 && !aligned16(codebook16)) return W4A16_ERR_INVALID_ARG;
   if (M <= W4A16_GEMV_MAX_M) {
     const GemvPlan p = gemv_plan(M, N, K, kNF4);
     st = check_workspace(p, workspace, workspace_bytes);
@@ -164,6 +164,7 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
     GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace, dev_status);
     a.absmax = absmax;
     a.codebook = codebook16;
+    a.cb_builtin = nf4_builtin_codebook();
     return from_cuda(launch_gemv_nf4(a, dtype == W4A16_BF16, stream));
   }
   st = check_gemm_workspace(gemm_split_plan(M, N, K, false), workspace, workspace_bytes);
@@ -173,6 +174,7 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
   a.qw = qweight;
   a.absmax = absmax;
   a.codebook = codebook16;
+  a.cb_builtin = nf4_builtin_codebook();
   a.Y = static_cast<uint16_t*>(Y);
   a.dev_status = dev_status;
   a.M = M;
@@ -203,7 +205,8 @@ w4a16_status nf4_dequant(const uint32_t* qweight, const float* absmax, const flo
   w4a16_status st = check_nf4_shape(0, N, K, blocksize);
   if (st != W4A16_OK) return st;
   if (N == 0) return W4A16_OK;
-  if (!ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(codebook16) || !ok_ptr(W_out)) return W4A16_ERR_INVALID_ARG;
+  if (!ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(W_out)) return W4A16_ERR_INVALID_ARG;
+  if (codebook16 && !aligned16(codebook16)) return W4A16_ERR_INVALID_ARG;
   return from_cuda(launch_dequant_nf4(qweight, absmax, codebook16, static_cast<uint16_t*>(W_out), K, N, blocksize,
                                       dtype == W4A16_BF16, stream));
 }
@@ -223,7 +226,8 @@ w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const flo
   w4a16_status st = check_nf4_shape(0, N, K, blocksize);
   if (st != W4A16_OK) return st;
   if (N == 0) return W4A16_OK;
-  if (!ok_ptr(W) || !ok_ptr(codebook16) || !ok_ptr(qweight) || !ok_ptr(absmax)) return W4A16_ERR_INVALID_ARG;
+  if (!ok_ptr(W) || !ok_ptr(qweight) || !ok_ptr(absmax)) return W4A16_ERR_INVALID_ARG;
+  if (codebook16 && !aligned16(codebook16)) return W4A16_ERR_INVALID_ARG;
   return from_cuda(launch_quantize_nf4(W, K, N, blocksize, codebook16, qweight, absmax, stream));
 }
 

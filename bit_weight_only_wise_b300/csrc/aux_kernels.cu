@@ -84,11 +84,11 @@ __global__ void __launch_bounds__(256) dequant_int4_kernel(const uint32_t* __res
 template <bool BF16>
 __global__ void __launch_bounds__(256) dequant_nf4_kernel(const uint32_t* __restrict__ qw,
                                                           const float* __restrict__ absmax,
-                                                          const float* __restrict__ codebook,
+                                                          const float* __restrict__ codebook, const Cb16 cb_builtin,
                                                           uint16_t* __restrict__ out, int K, int N,
                                                           int blocksize) {
   __shared__ float cb[16];
-  if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
+  if (threadIdx.x < 16) cb[threadIdx.x] = codebook ? codebook[threadIdx.x] : cb_builtin.v[threadIdx.x];
   __syncthreads();
   const int n4 = blockIdx.x * blockDim.x + threadIdx.x;
   const int i = blockIdx.y;
@@ -168,10 +168,10 @@ __global__ void __launch_bounds__(256) quantize_rtn_kernel(const float* __restri
 // ------------------------------------------------------------ quantize NF4
 __global__ void __launch_bounds__(256) quantize_nf4_kernel(const float* __restrict__ W, int K, int N,
                                                            int blocksize, const float* __restrict__ codebook,
-                                                           uint32_t* __restrict__ qw,
+                                                           const Cb16 cb_builtin, uint32_t* __restrict__ qw,
                                                            float* __restrict__ absmax) {
   __shared__ double cb[16];
-  if (threadIdx.x < 16) cb[threadIdx.x] = (double)codebook[threadIdx.x];
+  if (threadIdx.x < 16) cb[threadIdx.x] = (double)(codebook ? codebook[threadIdx.x] : cb_builtin.v[threadIdx.x]);
   __syncthreads();
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const int b = blockIdx.y;
@@ -222,8 +222,9 @@ cudaError_t launch_dequant_int4(const uint32_t* qw, const uint16_t* scales, cons
 cudaError_t launch_dequant_nf4(const uint32_t* qw, const float* absmax, const float* codebook, uint16_t* out,
                                int K, int N, int blocksize, bool bf16, cudaStream_t st) {
   dim3 block(256), grid((N / 4 + 255) / 256, K / 8);
-  if (bf16) dequant_nf4_kernel<true><<<grid, block, 0, st>>>(qw, absmax, codebook, out, K, N, blocksize);
-  else dequant_nf4_kernel<false><<<grid, block, 0, st>>>(qw, absmax, codebook, out, K, N, blocksize);
+  const Cb16& cb = nf4_builtin_codebook();
+  if (bf16) dequant_nf4_kernel<true><<<grid, block, 0, st>>>(qw, absmax, codebook, cb, out, K, N, blocksize);
+  else dequant_nf4_kernel<false><<<grid, block, 0, st>>>(qw, absmax, codebook, cb, out, K, N, blocksize);
   return cudaGetLastError();
 }
 
@@ -237,7 +238,7 @@ cudaError_t launch_quantize_rtn(const float* W, int K, int N, int group_size, ui
 cudaError_t launch_quantize_nf4(const float* W, int K, int N, int blocksize, const float* codebook, uint32_t* qw,
                                 float* absmax, cudaStream_t st) {
   dim3 block(256), grid((N + 255) / 256, K / blocksize);
-  quantize_nf4_kernel<<<grid, block, 0, st>>>(W, K, N, blocksize, codebook, qw, absmax);
+  quantize_nf4_kernel<<<grid, block, 0, st>>>(W, K, N, blocksize, codebook, nf4_builtin_codebook(), qw, absmax);
   return cudaGetLastError();
 }
 

@@ -101,7 +101,8 @@ struct GemmParams {
   const uint16_t* scales;
   const uint32_t* qz;
   const float* absmax;
-  const float* codebook;
+  const float* codebook;  // device table, or nullptr: cb_builtin
+  Cb16 cb_builtin;
   uint16_t* Y;
   int* dev_status;
   int M, N, K;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
   }
-  if (FMT == kFmtNF4 && threadIdx.x < 16) bars->cb[threadIdx.x] = p.codebook[threadIdx.x];
+  if (FMT == kFmtNF4 && threadIdx.x < 16) bars->cb[threadIdx.x] = p.codebook ? p.codebook[threadIdx.x] : p.cb_builtin.v[threadIdx.x];
   if (FMT == kFmtInt4Act) {
     const int G = p.K / 128;
     for (int i = threadIdx.x; i < G * kBN; i += kThreads) {
@@ -480,6 +481,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   p.qz = a.qz;
   p.absmax = a.absmax;
   p.codebook = a.codebook;
+  p.cb_builtin = a.cb_builtin;
   p.Y = a.Y;
   p.dev_status = a.dev_status;
   p.M = a.M;

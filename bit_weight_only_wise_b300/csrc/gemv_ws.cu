@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kWsThreads, 2)
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (FMT == kNF4 && threadIdx.x < 16) s_cb[threadIdx.x] = a.codebook[threadIdx.x];
+  if (FMT == kNF4 && threadIdx.x < 16) s_cb[threadIdx.x] = a.codebook ? a.codebook[threadIdx.x] : a.cb_builtin.v[threadIdx.x];
   __syncthreads();
   volatile int* abort = &abort_flag;
   if (warp == kProducer)

@@ -12,6 +12,14 @@ namespace w4a16 {
 // workspace size can be computed on the host without a device query.
 constexpr int kNumSMs = 148;
 
+// A 16-entry NF4 table passed to kernels by value (used when the caller gives
+// no table of its own).
+struct Cb16 {
+  float v[16];
+};
+// The library's built-in NF4 table (host; built once per process).
+const Cb16& nf4_builtin_codebook();
+
 // ----------------------------------------------------------- split-K GEMV
 constexpr int kGemvThreads = 256;            // 8 warps, one 32-column slice each
 constexpr int kGemvCols = 256;               // columns per unit
@@ -43,7 +51,8 @@ struct GemvArgs {
   const uint32_t* qz;      // INT4 packed zeros
   const int32_t* g_idx;    // INT4 act-order map or nullptr
   const float* absmax;     // NF4
-  const float* codebook;   // NF4
+  const float* codebook;   // NF4 table in device memory, or nullptr: cb_builtin
+  Cb16 cb_builtin;         // NF4 table used when codebook is nullptr
   uint16_t* Y;
   float* partial;
   int* counters;
@@ -68,7 +77,8 @@ struct GemmArgs {
   const uint32_t* qz;      // INT4
   const int32_t* g_idx;    // INT4 act-order map or nullptr
   const float* absmax;     // NF4
-  const float* codebook;   // NF4
+  const float* codebook;   // NF4 table in device memory, or nullptr: cb_builtin
+  Cb16 cb_builtin;
   uint16_t* Y;
   int* dev_status;
   int M, N, K;
@@ -113,6 +123,7 @@ cudaError_t launch_gather_columns(const uint16_t* X, const int32_t* perm, int M,
 cudaError_t launch_dequant_int4(const uint32_t* qw, const uint16_t* scales, const uint32_t* qz,
                                 const int32_t* g_idx, uint16_t* out, int K, int N, int group_size,
                                 bool bf16, cudaStream_t st);
+// codebook: a device table, or nullptr for the built-in one
 cudaError_t launch_dequant_nf4(const uint32_t* qw, const float* absmax, const float* codebook, uint16_t* out,
                                int K, int N, int blocksize, bool bf16, cudaStream_t st);
 cudaError_t launch_quantize_rtn(const float* W, int K, int N, int group_size, uint32_t* qw, uint16_t* scales,

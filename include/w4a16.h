@@ -36,7 +36,8 @@
  *                      word [g, c] (packed along N; the stored value is z)
  *   g_idx   int32 [K]  row -> group, each value in [0, K/128); NULL means k/128
  *   absmax  fp32 [K/64, N]                  (NF4)
- *   codebook16 fp32 [16], ascending         (NF4)
+ *   codebook16 fp32 [16], ascending         (NF4; NULL = the built-in table,
+ *                      see nf4_default_codebook)
  *
  * Conventions shared by every entry point:
  *  - Every pointer is a device pointer owned by the caller.  The library
@@ -128,7 +129,8 @@ w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scal
                         cudaStream_t stream);
 
 /* Y = X . W_hat for the NF4 format, any M >= 0.  blocksize: 64.
- * codebook16 must not be NULL.  Other arguments as w4a16_gemm. */
+ * codebook16: a device table of 16 fp32 values, or NULL for the library's
+ * built-in table (nf4_default_codebook).  Other arguments as w4a16_gemm. */
 w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absmax,
                       const float* codebook16, void* Y, int M, int N, int K, int blocksize,
                       w4a16_dtype dtype, void* workspace, size_t workspace_bytes,
@@ -140,7 +142,8 @@ w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales, const ui
                            const int32_t* g_idx, void* W_out, int K, int N, int group_size,
                            w4a16_dtype dtype, cudaStream_t stream);
 
-/* W_out[K, N] (dtype) = W_hat for NF4; bit-exact with the definition above. */
+/* W_out[K, N] (dtype) = W_hat for NF4; bit-exact with the definition above.
+ * codebook16: as nf4_gemm (NULL = built-in table). */
 w4a16_status nf4_dequant(const uint32_t* qweight, const float* absmax, const float* codebook16,
                          void* W_out, int K, int N, int blocksize, w4a16_dtype dtype,
                          cudaStream_t stream);
@@ -164,6 +167,7 @@ w4a16_status w4a16_quantize(const float* W, int K, int N, int group_size, uint32
  * column; v = fl32(w / absmax); q = the index of the codebook entry nearest
  * to v (exact comparison, ties to the lower index; code 7 for an all-zero
  * block).  Outputs qweight [K/8, N] and absmax fp32 [K/64, N].
+ * codebook16: as nf4_gemm (NULL = built-in table).
  */
 w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const float* codebook16,
                           uint32_t* qweight, float* absmax, cudaStream_t stream);
@@ -250,6 +254,23 @@ size_t w4a16_prepacked_workspace_bytes(int M, int N, int K);
  * dev_status must not be NULL.
  */
 w4a16_status w4a16_selftest_wait_timeout(int* dev_status, unsigned long long limit_ns, cudaStream_t stream);
+
+/*
+ * The library's built-in NF4 table, written to out16[0..15] (host memory):
+ * the table NULL stands for in nf4_gemm, nf4_dequant and nf4_quantize.  NF4
+ * places its 16 values where normally distributed weights are dense
+ * ("LLM量化技术深度对比" key-data item 2; "GPTQ、AWQ与Bitsandbytes" §2.3:
+ * built from a normal-distribution prior).  With d = 1 - (1/30 + 1/32) / 2
+ * and Phi the standard-normal CDF:
+ *   C[7] = 0,
+ *   C[8 + i] =  Phi^-1(d - (d - 1/2) i / 8) / Phi^-1(d),   i = 0..7,
+ *   C[6 - i] = -Phi^-1(d - (d - 1/2) i / 7) / Phi^-1(d),   i = 0..6,
+ * each quotient formed in double and rounded once to fp32 (C[0] = -1,
+ * C[15] = 1, ascending).  The pages print no table; equality with any other
+ * library's shipped table is not claimed.  Pure host function;
+ * W4A16_ERR_INVALID_ARG if out16 is NULL.
+ */
+w4a16_status nf4_default_codebook(float* out16);
 
 /* Static, human-readable text for a status code.  Pure host function. */
 const char* w4a16_status_string(w4a16_status status);

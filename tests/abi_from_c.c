@@ -89,6 +89,7 @@ int main(void) {
       (fn_t)w4a16_workspace_bytes, (fn_t)w4a16_act_order_prepack,
       (fn_t)w4a16_gemm_prepacked, (fn_t)w4a16_prepacked_workspace_bytes,
       (fn_t)w4a16_selftest_wait_timeout, (fn_t)w4a16_status_string,
+      (fn_t)nf4_default_codebook,
   };
   for (size_t i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i) CHECK(fns[i] != NULL);
 
@@ -101,6 +102,15 @@ int main(void) {
   CHECK(w4a16_workspace_bytes(0, 4096, 4096) == 0);
   CHECK(w4a16_workspace_bytes(1, 4096, 4096) == w4a16_workspace_bytes(1, 4096, 4096));
   CHECK(w4a16_prepacked_workspace_bytes(4, 64, 256) >= (size_t)4 * 256 * 2);
+
+  /* the built-in NF4 table: -1 .. 1, zero at index 7, ascending */
+  {
+    float cb[16];
+    CHECK(nf4_default_codebook(cb) == W4A16_OK);
+    CHECK(cb[0] == -1.0f && cb[7] == 0.0f && cb[15] == 1.0f);
+    for (int i = 1; i < 16; ++i) CHECK(cb[i] > cb[i - 1]);
+    CHECK(nf4_default_codebook(NULL) == W4A16_ERR_INVALID_ARG);
+  }
 
   /* validation: rejected before any launch */
   CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, 64, 256, 128, (w4a16_dtype)7, NULL, 0, NULL,

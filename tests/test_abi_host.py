@@ -41,6 +41,22 @@ def test_library_exports_every_declared_symbol(lib):
         assert name in w4.EXPORTED, name
 
 
+def test_builtin_nf4_codebook_equals_the_oracles(lib):
+    # the library's own table (host code, Newton's method on libm's erfc) and
+    # the oracle's (scipy's normal quantile) are bit-identical fp32 tables
+    import ctypes
+
+    import numpy as np
+
+    from oracle import nf4
+
+    buf = (ctypes.c_float * 16)()
+    assert lib.nf4_default_codebook(ctypes.addressof(buf)) == 0
+    got = np.frombuffer(bytes(buf), dtype=np.float32)
+    assert np.array_equal(got.view(np.uint32), nf4.codebook().view(np.uint32))
+    assert lib.nf4_default_codebook(None) == 1  # NULL destination: invalid argument
+
+
 def test_status_strings(lib):
     import bit_weight_only_wise_b300 as w4
 
@@ -78,13 +94,17 @@ def test_validation_rejects_without_launch(lib):
         assert _gemm(lib, K=256 * 32, ws=None, wsb=0) == INV
         assert _gemm(lib, K=256 * 32, ws=16, wsb=need - 1) == INV
     # NF4
-    assert lib.nf4_gemm(16, 16, 16, None, 16, 4, 64, 256, 64, 1, None, 0, None, None) == INV  # codebook
+    # a codebook is optional (NULL: the built-in table) but must be aligned
+    assert lib.nf4_gemm(16, 16, 16, 8, 16, 4, 64, 256, 64, 1, None, 0, None, None) == INV
+    assert lib.nf4_gemm(16, 16, None, None, 16, 4, 64, 256, 64, 1, None, 0, None, None) == INV  # absmax
     assert lib.nf4_gemm(16, 16, 16, 16, 16, 4, 64, 256, 32, 1, None, 0, None, None) == UNS
     assert lib.nf4_gemm(16, 16, 16, 16, 16, 4, 64, 100, 64, 1, None, 0, None, None) == INV
     assert lib.w4a16_dequant(16, 16, 16, None, 16, 256, 60, 128, 0, None) == INV
-    assert lib.nf4_dequant(16, 16, None, 16, 256, 64, 64, 0, None) == INV
+    assert lib.nf4_dequant(16, 16, 8, 16, 256, 64, 64, 0, None) == INV
+    assert lib.nf4_dequant(16, None, None, 16, 256, 64, 64, 0, None) == INV
     assert lib.w4a16_quantize(None, 256, 64, 128, 16, 16, 16, None) == INV
-    assert lib.nf4_quantize(16, 256, 64, 64, None, 16, 16, None) == INV
+    assert lib.nf4_quantize(16, 256, 64, 64, 8, 16, 16, None) == INV
+    assert lib.nf4_quantize(16, 256, 64, 64, None, 16, None, None) == INV
     # the wait self-test needs a status word and a limit in (0, 10 s]
     assert lib.w4a16_selftest_wait_timeout(None, 1000, None) == INV
     assert lib.w4a16_selftest_wait_timeout(16, 0, None) == INV

@@ -6,8 +6,9 @@ import torch
 
 import bit_weight_only_wise_b300 as w4
 from oracle import int4, nf4
-from synth import WORKLOADS, act_order_g_idx, gaussian_weights, student_t_weights, weights_for
+from synth import WORKLOADS, act_order_g_idx, activations, gaussian_weights, student_t_weights, weights_for
 
+import gpu_util
 from gpu_util import bits, dev, to_dev, to_dev_u32
 
 pytestmark = pytest.mark.gpu
@@ -96,7 +97,32 @@ def test_nf4_quantize_matches_oracle():
 
 
 def test_binding_codebook_matches_oracle_codebook():
-    # the binding computes its default table independently (torch ndtri)
+    # the library builds its default table independently of the oracle (its own
+    # Newton iteration on libm's erfc); the two fp32 tables are bit-identical
     got = w4.nf4_codebook(dev()).cpu().numpy()
     want = nf4.codebook()
-    assert np.all(np.abs(got - want) <= np.spacing(np.abs(want)))
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_nf4_null_codebook_is_the_builtin_table():
+    # a NULL table in the C calls means the built-in one: quantize, dequantize
+    # and both product kernels give bit-identical results with NULL and with
+    # the oracle's table passed explicitly
+    K, N = 512, 264
+    W = gaussian_weights(K, N, 0.02, 12)
+    cb = nf4.codebook()
+    Wd, cbd = to_dev(W), to_dev(cb)
+    qw0, am0 = w4.nf4_quantize(Wd, None)
+    qw1, am1 = w4.nf4_quantize(Wd, cbd)
+    assert torch.equal(qw0, qw1) and torch.equal(am0, am1)
+    qw_o, am_o, codes = nf4.nf4_quantize_packed(W, cb)
+    assert np.array_equal(qw0.cpu().numpy().view(np.uint32), qw_o)
+    for dt in ("bf16", "f16"):
+        d0 = w4.nf4_dequant(qw0, am0, None, dtype=gpu_util.TDT[dt])
+        assert np.array_equal(bits(d0), nf4.nf4_dequant(codes, am_o, cb, dt))
+        for M in (3, 40):
+            X = activations(M, K, dt, 5).to(dev())
+            y0 = w4.nf4_gemm(X, qw0, am0, None)
+            y1 = w4.nf4_gemm(X, qw0, am0, cbd)
+            torch.cuda.synchronize()
+            assert torch.equal(y0, y1)
