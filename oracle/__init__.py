@@ -17,6 +17,8 @@ weight-only quantization describe:
 * ``product``   -- the fp64 reference product Y = X . W_hat and the
                    tolerance checks used by the parity tests.
 * ``accounting``-- byte counts of the packed checkpoint tensors.
+* ``awq``       -- the AWQ checkpoint layout (codes packed along N in AWQ's
+                   column order) and its re-arrangement into this layout.
 
 Floating point work is done in fp64 unless a step is defined in a narrower
 type (the fp16 scale, the fp32 NF4 product).  Every function names the
@@ -27,7 +29,9 @@ numerics, int4, product and accounting are pinned by the tests under
 ``tests/test_oracle_*.py``.  The NF4 codebook is pinned by its invariants and
 an independent bisection of the normal CDF; exact equality of that codebook
 with the table shipped by bitsandbytes is *parity unpinned*, because the pages
-do not print the table.
+do not print the table; so is equality of the NF4 double-quantization second
+level with bitsandbytes', and of the AWQ layout with files written by AWQ's
+own tools (the pages describe neither).
 """
 
-from . import accounting, int4, nf4, numerics, product  # noqa: F401
+from . import accounting, awq, int4, nf4, numerics, product  # noqa: F401

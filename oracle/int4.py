@@ -30,6 +30,13 @@ Readings where the pages are silent (each listed in the design notes):
 6. Dequantization: ``w_hat = (q - z) * s`` is exact in fp32 (|q - z| <= 15
    has 4 bits, ``s`` 11); the value used by the product is that exact value
    rounded once to the compute dtype.
+7. Symmetric quantization (cloud.tencent.com/developer/article/2726413 §2.1:
+   the float range is mapped symmetrically onto the integer range and the
+   zero point is fixed at 0): signed 4-bit codes ``c`` in [-8, 7] with
+   ``s = fp16_RNE(max |w| / 7)`` (a zero scale becomes 1) and
+   ``c = clamp(rint(w / s), -8, 7)``, stored in the same unsigned nibble as
+   ``q = c + 8``; so the stored format is the asymmetric one with every zero
+   point equal to 8, and no zero points need to be stored.
 """
 
 from __future__ import annotations
@@ -79,6 +86,39 @@ def rtn_quantize(W: np.ndarray, group_size: int = 128, g_idx=None):
         scales[gi] = s16
         zeros[gi] = z.astype(np.uint8)
     return q, scales, zeros
+
+
+SYM_ZERO = 8
+
+
+def rtn_quantize_sym(W: np.ndarray, group_size: int = 128, g_idx=None):
+    """Symmetric RTN quantization of fp32 ``W[K, N]`` (reading 7).
+
+    Returns ``(q uint8[K, N], scales float16[G, N])``; the zero point of every
+    group is ``SYM_ZERO`` (8).
+    """
+    W = np.asarray(W, dtype=np.float32)
+    K, N = W.shape
+    gid = row_groups(K, group_size, g_idx)
+    G = K // group_size
+    q = np.empty((K, N), dtype=np.uint8)
+    scales = np.empty((G, N), dtype=np.float16)
+    for gi in range(G):
+        rows = np.nonzero(gid == gi)[0]
+        Wg = W[rows].astype(np.float64)
+        amax = np.abs(Wg).max(axis=0)
+        s16 = numerics.to_f16(amax / 7.0)
+        s16[s16 == 0] = np.float16(1.0)
+        s = s16.astype(np.float64)
+        c = np.clip(np.rint(Wg / s), -8, 7)
+        q[rows] = (c + SYM_ZERO).astype(np.uint8)
+        scales[gi] = s16
+    return q, scales
+
+
+def sym_zeros(G: int, N: int) -> np.ndarray:
+    """The zero points a symmetric checkpoint implies: 8 everywhere."""
+    return np.full((G, N), SYM_ZERO, dtype=np.uint8)
 
 
 def pack_along_k(q: np.ndarray) -> np.ndarray:

@@ -31,6 +31,24 @@ notes):
 
 Equality of this codebook with the table bitsandbytes ships is parity
 unpinned: the pages do not print that table.
+
+Double quantization ("GPTQ、AWQ与Bitsandbytes" §3.3 sets
+``bnb_4bit_use_double_quant=True``; its pitfall list in §4.3 explains that
+double quantization stores a scale of the scale).  Reading, where the pages
+stop there:
+
+5. The fp32 absmax values are themselves quantized to 8-bit unsigned codes
+   (absmax >= 0), in blocks of 256 consecutive values of one absmax row
+   (256 consecutive output columns of one 64-row block), each block with one
+   fp32 second-level scale ``s2 = fl32(max / 255)`` (a zero scale becomes 1),
+   ``code = clamp(rint(absmax / s2), 0, 255)`` (division in fp64).
+6. The stored absmax is then ``absmax_hat = fl32(code * s2)`` (one fp32
+   rounding of the exact product), and the weights' 4-bit codes are those of
+   the first level, computed with the original absmax; dequantization uses
+   ``absmax_hat`` in place of absmax.
+
+Equality of this second level with bitsandbytes' own (which the pages do not
+describe) is parity unpinned.
 """
 
 from __future__ import annotations
@@ -104,6 +122,37 @@ def nf4_dequant(codes, absmax, cb, dtype: str = "bf16", blocksize: int = 64) -> 
     c = np.asarray(cb, dtype=np.float32)[codes]
     prod = (c * am).astype(np.float32)  # one fp32 rounding
     return numerics.round_to_dtype_bits(prod, dtype)
+
+
+DQ_BLOCK = 256
+
+
+def double_quantize_absmax(absmax: np.ndarray, dq_block: int = DQ_BLOCK):
+    """Second-level quantization of fp32 ``absmax[B, N]`` (readings 5 and 6):
+    ``(codes uint8[B, N], s2 float32[B, ceil(N / dq_block)])``."""
+    am = np.asarray(absmax, dtype=np.float32)
+    B, N = am.shape
+    nc = -(-N // dq_block)
+    codes = np.empty((B, N), dtype=np.uint8)
+    s2 = np.empty((B, nc), dtype=np.float32)
+    for c in range(nc):
+        blk = am[:, c * dq_block:(c + 1) * dq_block].astype(np.float64)
+        s = (blk.max(axis=1) / 255.0).astype(np.float32)  # one rounding of the fp64 quotient
+        s[s == 0] = np.float32(1.0)
+        s2[:, c] = s
+        codes[:, c * dq_block:(c + 1) * dq_block] = np.clip(
+            np.rint(blk / s.astype(np.float64)[:, None]), 0, 255).astype(np.uint8)
+    return codes, s2
+
+
+def absmax_from_double_quant(codes: np.ndarray, s2: np.ndarray, dq_block: int = DQ_BLOCK) -> np.ndarray:
+    """``absmax_hat = fl32(code * s2)`` as float32 ``[B, N]``."""
+    codes = np.asarray(codes)
+    B, N = codes.shape
+    s = np.repeat(np.asarray(s2, dtype=np.float32), dq_block, axis=1)[:, :N]
+    # code (<= 255) and s2 are exact in fp64, so the fp64 product is exact and
+    # its conversion to float32 is the single rounding
+    return (codes.astype(np.float64) * s.astype(np.float64)).astype(np.float32)
 
 
 def nf4_quantize_packed(W, cb, blocksize: int = 64):

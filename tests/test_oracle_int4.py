@@ -247,3 +247,57 @@ def test_range_always_contains_zero():
     # and in both, the weights come back exactly
     assert np.array_equal(int4.dequant_exact(q, s, z), W.astype(np.float64))
     assert np.array_equal(int4.dequant_exact(qn, sn, zn), -W.astype(np.float64))
+
+
+# ---------------------------------------------------------------- symmetric
+def test_symmetric_exact_grid_recovered():
+    # Symmetric quantization (same passage, §2.1): the range [-max|w|, max|w|]
+    # maps onto the signed integers with the zero point fixed at 0.  Weights
+    # c * u with c in -7..7 and max |w| = 7u (u = 2^-8, exact in fp16) come
+    # back as scale u and stored codes c + 8.
+    u = 2.0 ** -8
+    rng = np.random.default_rng(5)
+    c0 = rng.integers(-7, 8, size=(256, 24))
+    c0[0] = 7
+    c0[1] = -7
+    W = (c0 * u).astype(np.float32)
+    q, s = int4.rtn_quantize_sym(W)
+    assert np.all(s.astype(np.float64) == u)
+    assert np.array_equal(q.astype(int), c0 + 8)
+    z = int4.sym_zeros(*s.shape)
+    assert np.array_equal(int4.dequant_exact(q, s, z), W.astype(np.float64))
+
+
+def test_symmetric_scale_is_max_abs_over_7_and_zero_is_exact():
+    # one group whose largest magnitude is negative: s = fp16(max|w| / 7) (here
+    # |min| = 0.0875 -> 0.0125 -> fp16 6552 * 2^-19 = 0.0124969482421875), the most negative
+    # weight gets code 8 - 7 = 1, and 0 gets code 8 and reconstructs to 0
+    W = np.zeros((128, 8), dtype=np.float32)
+    W[0] = -0.0875
+    W[1] = 0.05
+    q, s = int4.rtn_quantize_sym(W)
+    assert np.all(s == np.float16(0.0125))
+    assert float(np.float16(0.0125)) == 6552 * 2.0 ** -19
+    assert np.all(q[0] == 1) and np.all(q[2:] == 8)
+    # 0.05 / 0.0124969 = 4.0010 -> 4 -> code 12; -0.0875 / 0.0124969 = -7.0017 -> -7
+    assert np.all(q[1] == 12)
+    w_hat = int4.dequant_exact(q, s, int4.sym_zeros(*s.shape))
+    assert np.all(w_hat[2:] == 0.0)
+
+
+def test_symmetric_is_odd_and_within_half_a_step():
+    K, N = 512, 64
+    W = student_t_weights(K, N, 5, 0.01, 8)
+    q, s = int4.rtn_quantize_sym(W)
+    qn, sn = int4.rtn_quantize_sym(-W)
+    assert np.array_equal(s, sn)
+    z = int4.sym_zeros(*s.shape)
+    w1 = int4.dequant_exact(q, s, z)
+    w2 = int4.dequant_exact(qn, sn, z)
+    assert np.array_equal(w2, -w1)  # w -> -w flips every reconstruction (rint is odd)
+    s_rows = s.astype(np.float64)[np.arange(K) // 128]
+    err = np.abs(W.astype(np.float64) - w1)
+    # |w / s| <= 7 (1 + 2^-11) < 7.5, so no code is clamped: half a step everywhere
+    assert np.all(err <= s_rows / 2)
+    ratio = w1 / s_rows
+    assert np.array_equal(ratio, np.round(ratio)) and np.all(np.abs(ratio) <= 7)

@@ -99,3 +99,53 @@ def test_dequant_is_fp32_product_then_one_rounding():
             pv = Fraction(float(p))
             best = min(zip(vals, cands), key=lambda t: (abs(t[0] - pv), t[1] % 2))[1]
             assert got[k, n] == best
+
+
+# ----------------------------------------------------- double quantization
+def test_double_quant_exact_grid_recovered():
+    # absmax values on the second-level grid k * s2, with each 256-column
+    # block's maximum at 255 * s2 (s2 = 2^-12, exact), come back unchanged:
+    # s2 = max / 255 exactly, codes k, absmax_hat = absmax
+    s2 = 2.0 ** -12
+    rng = np.random.default_rng(2)
+    B, N = 6, 600  # three second-level blocks per row, the last one ragged
+    k = rng.integers(0, 256, size=(B, N))
+    k[:, 0] = 255
+    k[:, 256] = 255
+    k[:, 512] = 255
+    am = (k * s2).astype(np.float32)
+    codes, sc = nf4.double_quantize_absmax(am)
+    assert sc.shape == (B, 3) and np.all(sc == np.float32(s2))
+    assert np.array_equal(codes.astype(int), k)
+    assert np.array_equal(nf4.absmax_from_double_quant(codes, sc), am)
+
+
+def test_double_quant_half_step_and_blocks():
+    W = gaussian_weights(1024, 520, 0.02, 4)
+    cb = nf4.codebook()
+    _, am = nf4.nf4_quantize(W, cb)
+    codes, sc = nf4.double_quantize_absmax(am)
+    hat = nf4.absmax_from_double_quant(codes, sc).astype(np.float64)
+    s_cols = np.repeat(sc.astype(np.float64), 256, axis=1)[:, :am.shape[1]]
+    # rint to the nearest step, then one fp32 rounding of code * s2
+    err = np.abs(hat - am.astype(np.float64))
+    assert np.all(err <= s_cols / 2 + np.spacing(hat.astype(np.float32)).astype(np.float64))
+    # each block's largest absmax takes code 255; the scale is per block of 256
+    # consecutive columns of one row: a change in one block moves only its s2
+    for c in range(sc.shape[1]):
+        blk = codes[:, c * 256:(c + 1) * 256]
+        assert np.all(blk.max(axis=1) == 255)
+    am2 = am.copy()
+    am2[3, 10] *= 2
+    _, sc2 = nf4.double_quantize_absmax(am2)
+    diff = np.argwhere(sc2 != sc)
+    assert diff.tolist() == [[3, 0]]
+
+
+def test_double_quant_zero_block():
+    am = np.zeros((2, 256), dtype=np.float32)
+    am[1, 5] = 0.5
+    codes, sc = nf4.double_quantize_absmax(am)
+    assert sc[0, 0] == 1.0 and np.all(codes[0] == 0)  # a zero scale becomes 1
+    hat = nf4.absmax_from_double_quant(codes, sc)
+    assert np.all(hat[0] == 0.0) and hat[1, 5] == np.float32(np.float32(0.5 / 255) * 255)
