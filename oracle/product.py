@@ -14,6 +14,18 @@ bit for bit), not against the exact (q - z) * s.
 
 Tolerances: per output, |Y - Y_ref| / sum_k |x_mk| |w_hat_kn| <= 1e-2, and
 over all checked outputs ||Y - Y_ref||_F / ||Y_ref||_F <= 2e-3.
+
+Fused MLP activation.  A decoder layer's gate_up projection is followed by
+SiLU(gate) * up before the down projection; per-token latency is the weight
+bytes streamed per forward ("LLM量化技术深度对比" key-data items 1 and 3), so
+the activation is applied as the product's epilogue instead of writing and
+re-reading the 2F-wide projection.  Readings (the pages do not spell the
+layer out): the gate_up weight is ``[K, 2F]`` with the gate in columns
+``[0, F)`` and the up projection in ``[F, 2F)``; ``SiLU(t) = t / (1 + e^-t)``;
+``act[m, j] = SiLU(y[m, j]) * y[m, F + j]`` with ``y = X . W_hat`` in fp64.
+Its tolerance uses the same two bounds with the normaliser carried through
+the activation to first order:
+``A_act = |SiLU'(g)| |u| A_g + |SiLU(g)| A_u``.
 """
 
 from __future__ import annotations
@@ -54,3 +66,27 @@ def within_tolerance(Y, Y_ref, A, max_rel: float = MAX_REL, fro_rel: float = FRO
     """``(ok, max_rel, fro_rel)``."""
     m, f = errors(Y, Y_ref, A)
     return (m <= max_rel and f <= fro_rel), m, f
+
+
+def silu(t):
+    """SiLU(t) = t / (1 + exp(-t)), fp64."""
+    t = np.asarray(t, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return t / (1.0 + np.exp(-t))
+
+
+def silu_grad(t):
+    """d/dt SiLU(t) = sigma(t) (1 + t (1 - sigma(t))), fp64."""
+    t = np.asarray(t, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        sg = 1.0 / (1.0 + np.exp(-t))
+    return sg * (1.0 + t * (1.0 - sg))
+
+
+def silu_mul_reference(X: np.ndarray, W_hat: np.ndarray):
+    """``(act_ref, A_act)`` for a gate_up weight ``W_hat[K, 2F]`` (gate first)."""
+    Y, A = reference(X, W_hat)
+    F = Y.shape[1] // 2
+    g, u = Y[:, :F], Y[:, F:]
+    Ag, Au = A[:, :F], A[:, F:]
+    return silu(g) * u, np.abs(silu_grad(g)) * np.abs(u) * Ag + np.abs(silu(g)) * Au

@@ -106,3 +106,36 @@ def test_workload_shapes_are_valid(name):
     wl = WORKLOADS[name]
     for K, N in wl.shapes:
         assert K % 128 == 0 and N % 8 == 0
+
+
+# ------------------------------------------------------ fused SiLU * up
+def test_silu_closed_forms():
+    t = np.array([-50.0, -3.0, -1e-3, 0.0, 1e-3, 2.0, 60.0])
+    s = product.silu(t)
+    assert s[3] == 0.0
+    # SiLU(t) - SiLU(-t) = t for every t (t sigma(t) + t (1 - sigma(t)))
+    assert np.allclose(product.silu(t) - product.silu(-t), t, rtol=0, atol=1e-15)
+    assert s[-1] == 60.0  # sigma(60) = 1 - 9e-27 rounds to 1 in fp64
+    assert 0 > s[0] > -1e-19  # -50 sigma(-50) = -50 e^-50 ~ -9.6e-21
+    assert abs(s[1] - (-3.0 / (1 + np.exp(3.0)))) < 1e-16
+    # derivative: central differences
+    h = 1e-6
+    for v in (-4.0, -0.5, 0.0, 0.7, 3.0):
+        fd = (product.silu(v + h) - product.silu(v - h)) / (2 * h)
+        assert abs(fd - product.silu_grad(v)) < 1e-8
+    assert product.silu_grad(0.0) == 0.5
+
+
+def test_silu_mul_takes_gate_first_then_up():
+    # K = 2, F = 3: gate columns are the first F, up the last F.  With X = [1, 0]
+    # the products are the first row of W itself.
+    W = np.array([[1.0, -2.0, 0.0, 3.0, 0.5, -1.0],
+                  [9.0, 9.0, 9.0, 9.0, 9.0, 9.0]])
+    act, A = product.silu_mul_reference(np.array([[1.0, 0.0]]), W)
+    sg = product.silu(np.array([1.0, -2.0, 0.0]))
+    assert np.allclose(act[0], sg * np.array([3.0, 0.5, -1.0]), rtol=1e-15, atol=0)
+    # normaliser: |SiLU'(g)| |u| A_g + |SiLU(g)| A_u with A = |x| |w|
+    Ag = np.array([1.0, 2.0, 0.0])
+    Au = np.array([3.0, 0.5, 1.0])
+    want = np.abs(product.silu_grad(np.array([1.0, -2.0, 0.0]))) * np.abs([3.0, 0.5, -1.0]) * Ag + np.abs(sg) * Au
+    assert np.allclose(A[0], want, rtol=1e-15, atol=0)
