@@ -16,7 +16,7 @@ shared generators, quantized on the GPU by the library's round-to-nearest
 kernel; the 64 layers are 64 distinct device copies of those four quantized
 linears (16.2 GB, far larger than the 126 MB L2, so no L2 flush is needed).
 
-* config sweep (``configs``): every workload's shapes and token counts (single
+* config sweep (``sweep``): every workload's shapes and token counts (single
   linear, decode sweep, act-order, Qwen shapes, NF4), each timed alone as a
   CUDA graph rotating through weight copies that exceed 4x L2; us per call,
   GB/s of algorithmic weight bytes, TFLOP/s and both roofline fractions.
@@ -122,17 +122,33 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_sample(seconds: float = 12.0):
-    """Oracle (dequantize + fp64 product) on the o projection at M=1, repeated
-    for about ``seconds``; returns (GB/s of packed weight bytes, cores, sample)."""
+# The oracle (dequantize + fp64 product), as it stands, on every host core:
+# the output columns are cut into one slab per core and each slab runs in its
+# own process (started with `spawn`, before this process touches the GPU), one
+# BLAS thread each.
+ORACLE_K, ORACLE_N = 5120, 5120  # the o projection of the Qwen2.5-32B-shaped stack
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _oracle_slab(job):
+    """Worker: quantize one column slab with the oracle, then repeat its
+    dequantization and product for ``seconds``; returns (passes, seconds, bytes
+    per pass, flops per pass)."""
+    c0, c1, M, seconds = job
     from oracle import int4, product
     from synth import activations, gaussian_weights
 
-    K, N = 5120, 5120
-    W = gaussian_weights(K, N, 0.02, 0)
+    K = ORACLE_K
+    W = gaussian_weights(K, ORACLE_N, 0.02, 0)[:, c0:c1]
     q, s, z = int4.rtn_quantize(W)
-    X = activations(1, K, "bf16", 1).double().numpy()
-    nbytes = int4_bytes(K, N)
+    X = activations(M, K, "bf16", 1).double().numpy()
+    n = c1 - c0
     done, t0 = 0, time.perf_counter()
     while True:
         w_hat = int4.dequant(q, s, z, "bf16")
@@ -141,14 +157,47 @@ def oracle_sample(seconds: float = 12.0):
         done += 1
         if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
-    try:
-        from threadpoolctl import threadpool_info
+    return done, time.perf_counter() - t0, int4_bytes(K, n), 2 * M * n * K
 
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        cores = 1
-    return nbytes * done / dt / 1e9, cores, f"o_proj 5120x5120 INT4 at M=1, {done} passes in {dt:.1f} s"
+
+def oracle_all_cores(seconds: float = 12.0, M: int = 1):
+    """The oracle on the o projection (5120 x 5120) at M tokens, one column slab
+    per host core, for about ``seconds``.  Returns (GB/s of packed weight bytes,
+    TFLOP/s, cores, sample description)."""
+    import multiprocessing as mp
+
+    cores = host_cores()
+    edges = [ORACLE_N * i // cores // 8 * 8 for i in range(cores)] + [ORACLE_N]
+    jobs = [(edges[i], edges[i + 1], M, seconds) for i in range(cores) if edges[i + 1] > edges[i]]
+    saved = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        with mp.get_context("spawn").Pool(len(jobs)) as pool:
+            res = pool.map(_oracle_slab, jobs)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    # every slab ran for about the same wall time; the job's rate is the sum
+    gbs = sum(d * b / t for d, t, b, _ in res) / 1e9
+    tflops = sum(d * f / t for d, t, _, f in res) / 1e12
+    passes = sum(d for d, _, _, _ in res)
+    sample = (f"o_proj {ORACLE_K}x{ORACLE_N} INT4 g128 at M={M}: dequantize + fp64 product, {len(jobs)} column "
+              f"slabs in parallel processes, {passes} slab passes in {seconds:.0f} s")
+    return gbs, tflops, len(jobs), sample
+
+
+def cpu_baselines(seconds: float):
+    """Decode (M = 1) and prefill (M = 4096, timed on 64 rows and scaled by
+    4096/64: the product's rows are independent) oracle rates on all cores."""
+    v, _, cores, sample = oracle_all_cores(seconds, 1)
+    _, tf64, _, sample64 = oracle_all_cores(max(2.0, seconds / 3), 64)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "prefill_tflops": round(tf64, 5),
+            "prefill_sample": sample64 + "; M=4096 extrapolated from these 64 rows (time x 4096/64)"}
 
 
 def run_reference(args):
@@ -158,27 +207,26 @@ def run_reference(args):
     steps, warm = args.steps, args.warmup
     per = max(2.0, 60.0 / max(1, steps + warm))
     for _ in range(warm):
-        oracle_sample(per / 2)
+        oracle_all_cores(per / 2)
     vals = []
     t0 = time.perf_counter()
     for _ in range(steps):
-        v, cores, sample = oracle_sample(per)
+        v, _, cores, sample = oracle_all_cores(per)
         vals.append(v)
     wall = time.perf_counter() - t0
     value = statistics.median(vals)
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": warm, "ms_per_step": round(wall * 1e3 / steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "CPU oracle (RTN INT4 dequantize + fp64 product), bounded sample of the "
                                "Qwen2.5-32B-shaped decode stack", "sample": sample},
-        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
-
 
 
 # ---------------------------------------------------- multi-rank (replicas)
@@ -263,6 +311,20 @@ def sweep_entry(name, K, N, M, dt, us, nbytes, hbm_peak, tc_peak):
             "GBs_incl_xy": round((nbytes + xy) / us / 1e3, 1), "TFLOPs": round(tf, 1),
             "hbm_frac": round(gbs / hbm_peak, 4), "tc_frac": round(tf / tc_peak, 4),
             "bound": "hbm" if M <= 16 else ("both" if M < 256 else "tensor")}
+
+
+def sweep_summary(entries):
+    """The sweep as one flat object of strings, one per timed configuration:
+    "<config> M=<M> KxN dtype" -> "<us> us, <GB/s> GB/s (<hbm frac>), <TFLOP/s>
+    TFLOP/s (<tensor frac>)" -- compact enough to sit in the bench line."""
+    if not entries:
+        return None
+    out = {}
+    for e in entries:
+        key = f"{e['config']} M={e['M']} {e['K']}x{e['N']} {e['dtype']}"
+        out[key] = (f"{e['us']} us, {e['GBs']} GB/s ({e['hbm_frac']:.3f} hbm), "
+                    f"{e['TFLOPs']} TFLOP/s ({e['tc_frac']:.3f} tc)")
+    return out
 
 
 def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
@@ -358,12 +420,18 @@ def traffic_from_profiles(kernel: str):
 
 
 def run_gpu(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    # the CPU baseline runs first: its worker processes start before this
+    # process makes any CUDA call
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baselines(args.cpu_seconds)
+
     import torch
 
     import bit_weight_only_wise_b300 as w4
     from synth import activations, gaussian_weights
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dist = None
@@ -500,12 +568,11 @@ def run_gpu(args):
             dist.destroy_process_group()
         return 0
 
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        v, cores, sample = oracle_sample(args.cpu_seconds)
-        cpu = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
-
     sweep = None if args.no_sweep else config_sweep(torch, w4, dev, hbm_peak, tc_peak)
+    if sweep:
+        # one line per timed configuration ahead of the bench line (for the log)
+        for e in sweep:
+            print(json.dumps({"sweep_entry": e}), flush=True)
 
     traffic = traffic_from_profiles("gemv_ws_kernel")
     achieved = per_gpu  # algorithmic bytes per launch / mean launch time == stack bytes / step time
@@ -565,7 +632,7 @@ def run_gpu(args):
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: pinned-host X -> device, 256 C-ABI calls through the Python binding, "
                        "outputs -> pinned host"},
-        "configs": sweep,
+        "sweep": sweep_summary(sweep),
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
