@@ -8,8 +8,8 @@ is no CPU fallback: if the library is missing, importing this package raises.
 Tensor conventions (all CUDA, contiguous):
   X        [M, K]  torch.float16 / torch.bfloat16
   qweight  [K/8, N] torch.int32 (bit pattern of the packed uint32 words)
-  scales   [K/128, N] torch.float16
-  qzeros   [K/128, N/8] torch.int32
+  scales   [K/g, N] torch.float16 (g = group_size: 32, 64, a multiple of 128, or K)
+  qzeros   [K/g, N/8] torch.int32, or None for symmetric weights
   g_idx    [K] torch.int32 or None
   absmax   [K/64, N] torch.float32 (NF4)
   codebook [16] torch.float32 (NF4), or None for the library's built-in table
@@ -51,6 +51,9 @@ _SIGS = {
     "w4a16_selftest_wait_timeout": [_vp, ctypes.c_ulonglong, _vp],
     "w4a16_status_string": [_i],
     "nf4_default_codebook": [_vp],
+    "nf4dq_gemm": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
+    "nf4dq_dequant": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
+    "nf4_double_quantize": [_vp, _i, _i, _i, _vp, _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -243,18 +246,57 @@ def nf4_dequant(qweight, absmax, codebook=None, dtype=torch.bfloat16, blocksize=
     return W
 
 
-def quantize(W, group_size=GROUP_SIZE):
-    """RTN INT4 quantization of fp32 CUDA ``W[K, N]`` -> (qweight, scales, qzeros)."""
+def quantize(W, group_size=GROUP_SIZE, symmetric=False):
+    """RTN INT4 quantization of fp32 CUDA ``W[K, N]`` -> (qweight, scales, qzeros);
+    ``symmetric``: no zero points (qzeros is None; every zero point is 8)."""
     if W.dtype != torch.float32 or not W.is_cuda or not W.is_contiguous():
         raise ValueError("W must be a contiguous CUDA float32 tensor")
     K, N = W.shape
     dev = W.device
     qweight = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
     scales = torch.empty((K // group_size, N), dtype=torch.float16, device=dev)
-    qzeros = torch.empty((K // group_size, N // 8), dtype=torch.int32, device=dev)
+    qzeros = None if symmetric else torch.empty((K // group_size, N // 8), dtype=torch.int32, device=dev)
     st = _lib.w4a16_quantize(_ptr(W), K, N, group_size, _ptr(qweight), _ptr(scales), _ptr(qzeros), _stream(dev))
     _check(st, "w4a16_quantize")
     return qweight, scales, qzeros
+
+
+def nf4dq_gemm(X, qweight, absmax_q, absmax_s2, codebook=None, out=None, blocksize=NF4_BLOCK, ws=None,
+               dev_status=None):
+    """Y = X . W_hat (NF4 with double-quantized absmax), any M."""
+    K = qweight.shape[0] * 8
+    N = qweight.shape[1]
+    _check_x(X, K)
+    M = X.shape[0]
+    Y = _out(X, N, out)
+    if ws is None:
+        ws = workspace(M, N, K, X.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _lib.nf4dq_gemm(_ptr(X), _ptr(qweight), _ptr(absmax_q), _ptr(absmax_s2), _ptr(codebook), _ptr(Y), M, N, K,
+                         blocksize, _DTYPES[X.dtype], _ptr(ws), nbytes, _ptr(dev_status), _stream(X.device))
+    _check(st, "nf4dq_gemm")
+    return Y
+
+
+def nf4_double_quantize(absmax, blocksize=NF4_BLOCK):
+    """Second-level quantization of an NF4 absmax [K/bs, N] -> (absmax_q uint8
+    [K/bs, N], absmax_s2 float32 [K/bs, ceil(N/256)])."""
+    B, N = absmax.shape
+    q = torch.empty((B, N), dtype=torch.uint8, device=absmax.device)
+    s2 = torch.empty((B, (N + 255) // 256), dtype=torch.float32, device=absmax.device)
+    st = _lib.nf4_double_quantize(_ptr(absmax), B * blocksize, N, blocksize, _ptr(q), _ptr(s2),
+                                  _stream(absmax.device))
+    _check(st, "nf4_double_quantize")
+    return q, s2
+
+
+def nf4dq_dequant(qweight, absmax_q, absmax_s2, codebook=None, dtype=torch.bfloat16, blocksize=NF4_BLOCK):
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    W = torch.empty((K, N), dtype=dtype, device=qweight.device)
+    st = _lib.nf4dq_dequant(_ptr(qweight), _ptr(absmax_q), _ptr(absmax_s2), _ptr(codebook), _ptr(W), K, N, blocksize,
+                            _DTYPES[dtype], _stream(qweight.device))
+    _check(st, "nf4dq_dequant")
+    return W
 
 
 def nf4_quantize(W, codebook=None, blocksize=NF4_BLOCK):

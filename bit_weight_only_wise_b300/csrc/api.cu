@@ -14,7 +14,6 @@ using namespace w4a16;
 
 namespace {
 
-constexpr int kInt4Group = 128;
 constexpr int kNF4Block = 64;
 static_assert(W4A16_MAX_K == 65535 * 8, "word-rows index a grid dimension");
 static_assert(W4A16_MAX_N == kMaxColBlocks * kGemvCols, "one split-K ticket slice per column block");
@@ -36,7 +35,7 @@ w4a16_status check_int4_shape(int M, int N, int K, int group_size) {
   if (M < 0 || N < 0 || K <= 0 || !in_limits(M, N, K)) return W4A16_ERR_INVALID_ARG;
   if (N % 8 || K % 8) return W4A16_ERR_INVALID_ARG;
   if (group_size <= 0 || K % group_size) return W4A16_ERR_INVALID_ARG;
-  if (group_size != kInt4Group) return W4A16_ERR_UNSUPPORTED;
+  if (!int4_group_supported(K, group_size)) return W4A16_ERR_UNSUPPORTED;
   return W4A16_OK;
 }
 
@@ -70,7 +69,7 @@ GemvArgs gemv_args(const void* X, const uint32_t* qw, void* Y, int M, int N, int
   a.M = M;
   a.N = N;
   a.K = K;
-  a.G = p.G;
+  a.KB = p.KB;
   a.blocks_n = p.blocks_n;
   a.ctas = p.ctas;
   a.counters = static_cast<int*>(ws);
@@ -79,7 +78,7 @@ GemvArgs gemv_args(const void* X, const uint32_t* qw, void* Y, int M, int N, int
 }
 
 w4a16_status int4_gemv_impl(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
-                            const int32_t* g_idx, void* Y, int M, int N, int K, w4a16_dtype dtype,
+                            const int32_t* g_idx, void* Y, int M, int N, int K, int group_size, w4a16_dtype dtype,
                             void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
   const GemvPlan p = gemv_plan(M, N, K, g_idx ? kInt4Act : kInt4);
   w4a16_status st = check_workspace(p, workspace, workspace_bytes);
@@ -88,14 +87,16 @@ w4a16_status int4_gemv_impl(const void* X, const uint32_t* qweight, const void* 
   a.scales = static_cast<const uint16_t*>(scales);
   a.qz = qzeros;
   a.g_idx = g_idx;
+  a.gsize = group_size;
+  a.NG = K / group_size;
   return from_cuda(launch_gemv_int4(a, dtype == W4A16_BF16, stream));
 }
 
+// qzeros may be NULL: symmetric weights (every zero point 8)
 w4a16_status check_int4_ptrs(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
                              const int32_t* g_idx, const void* Y) {
-  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(qzeros) || !ok_ptr(Y))
-    return W4A16_ERR_INVALID_ARG;
-  if (g_idx && !aligned16(g_idx)) return W4A16_ERR_INVALID_ARG;
+  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(Y)) return W4A16_ERR_INVALID_ARG;
+  if ((qzeros && !aligned16(qzeros)) || (g_idx && !aligned16(g_idx))) return W4A16_ERR_INVALID_ARG;
   return W4A16_OK;
 }
 
@@ -113,8 +114,8 @@ w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scal
   if (M == 0 || N == 0) return W4A16_OK;
   st = check_int4_ptrs(X, qweight, scales, qzeros, g_idx, Y);
   if (st != W4A16_OK) return st;
-  return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
-                        dev_status, stream);
+  return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, group_size, dtype, workspace,
+                        workspace_bytes, dev_status, stream);
 }
 
 w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
@@ -127,9 +128,9 @@ w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scal
   st = check_int4_ptrs(X, qweight, scales, qzeros, g_idx, Y);
   if (st != W4A16_OK) return st;
   if (M <= W4A16_GEMV_MAX_M)
-    return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, dtype, workspace, workspace_bytes,
-                          dev_status, stream);
-  if (g_idx && !gemm_act_order_fits(K)) return W4A16_ERR_UNSUPPORTED;
+    return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, group_size, dtype, workspace,
+                          workspace_bytes, dev_status, stream);
+  if (g_idx && !gemm_act_order_fits(K / group_size)) return W4A16_ERR_UNSUPPORTED;
   st = check_gemm_workspace(gemm_split_plan(M, N, K, g_idx != nullptr), workspace, workspace_bytes);
   if (st != W4A16_OK) return st;
   GemmArgs a{};
@@ -143,19 +144,29 @@ w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scal
   a.M = M;
   a.N = N;
   a.K = K;
+  a.gsize = group_size;
+  a.NG = K / group_size;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   return from_cuda(launch_gemm_tc(a, dtype == W4A16_BF16, false, stream));
 }
 
-w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absmax, const float* codebook16,
-                      void* Y, int M, int N, int K, int blocksize, w4a16_dtype dtype, void* workspace,
-                      size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// NF4 product with fp32 absmax (absmax_q == nullptr) or double-quantized
+// absmax (absmax_q, absmax_s2); validation common to both entry points.
+w4a16_status nf4_gemm_impl(const void* X, const uint32_t* qweight, const float* absmax, const uint8_t* absmax_q,
+                           const float* absmax_s2, const float* codebook16, void* Y, int M, int N, int K,
+                           int blocksize, w4a16_dtype dtype, void* workspace, size_t workspace_bytes,
+                           int* dev_status, cudaStream_t stream) {
   if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
   w4a16_status st = check_nf4_shape(M, N, K, blocksize);
   if (st != W4A16_OK) return st;
   if (M == 0 || N == 0) return W4A16_OK;
-  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(absmax) || !ok_ptr(Y)) return W4A16_ERR_INVALID_ARG;
+  if (!ok_ptr(X) || !ok_ptr(qweight) || !ok_ptr(Y)) return W4A16_ERR_INVALID_ARG;
+  if (absmax_q ? (!ok_ptr(absmax_q) || !ok_ptr(absmax_s2)) : !ok_ptr(absmax)) return W4A16_ERR_INVALID_ARG;
   if (codebook16 && !aligned16(codebook16)) return W4A16_ERR_INVALID_ARG;
   if (M <= W4A16_GEMV_MAX_M) {
     const GemvPlan p = gemv_plan(M, N, K, kNF4);
@@ -163,6 +174,8 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
     if (st != W4A16_OK) return st;
     GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace, dev_status);
     a.absmax = absmax;
+    a.absmax_q = absmax_q;
+    a.absmax_s2 = absmax_s2;
     a.codebook = codebook16;
     a.cb_builtin = nf4_builtin_codebook();
     return from_cuda(launch_gemv_nf4(a, dtype == W4A16_BF16, stream));
@@ -173,6 +186,8 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
   a.X = X;
   a.qw = qweight;
   a.absmax = absmax;
+  a.absmax_q = absmax_q;
+  a.absmax_s2 = absmax_s2;
   a.codebook = codebook16;
   a.cb_builtin = nf4_builtin_codebook();
   a.Y = static_cast<uint16_t*>(Y);
@@ -185,6 +200,47 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
   return from_cuda(launch_gemm_tc(a, dtype == W4A16_BF16, true, stream));
 }
 
+}  // namespace
+
+extern "C" {
+
+w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absmax, const float* codebook16,
+                      void* Y, int M, int N, int K, int blocksize, w4a16_dtype dtype, void* workspace,
+                      size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  return nf4_gemm_impl(X, qweight, absmax, nullptr, nullptr, codebook16, Y, M, N, K, blocksize, dtype, workspace,
+                       workspace_bytes, dev_status, stream);
+}
+
+w4a16_status nf4dq_gemm(const void* X, const uint32_t* qweight, const uint8_t* absmax_q, const float* absmax_s2,
+                        const float* codebook16, void* Y, int M, int N, int K, int blocksize, w4a16_dtype dtype,
+                        void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+  if (!absmax_q) return W4A16_ERR_INVALID_ARG;
+  return nf4_gemm_impl(X, qweight, nullptr, absmax_q, absmax_s2, codebook16, Y, M, N, K, blocksize, dtype,
+                       workspace, workspace_bytes, dev_status, stream);
+}
+
+w4a16_status nf4_double_quantize(const float* absmax, int K, int N, int blocksize, uint8_t* absmax_q,
+                                 float* absmax_s2, cudaStream_t stream) {
+  w4a16_status st = check_nf4_shape(0, N, K, blocksize);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(absmax) || !ok_ptr(absmax_q) || !ok_ptr(absmax_s2)) return W4A16_ERR_INVALID_ARG;
+  return from_cuda(launch_double_quantize(absmax, K / blocksize, N, absmax_q, absmax_s2, stream));
+}
+
+w4a16_status nf4dq_dequant(const uint32_t* qweight, const uint8_t* absmax_q, const float* absmax_s2,
+                           const float* codebook16, void* W_out, int K, int N, int blocksize, w4a16_dtype dtype,
+                           cudaStream_t stream) {
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_nf4_shape(0, N, K, blocksize);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(qweight) || !ok_ptr(absmax_q) || !ok_ptr(absmax_s2) || !ok_ptr(W_out)) return W4A16_ERR_INVALID_ARG;
+  if (codebook16 && !aligned16(codebook16)) return W4A16_ERR_INVALID_ARG;
+  return from_cuda(launch_dequant_nf4dq(qweight, absmax_q, absmax_s2, codebook16, static_cast<uint16_t*>(W_out), K,
+                                        N, blocksize, dtype == W4A16_BF16, stream));
+}
+
 w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
                            const int32_t* g_idx, void* W_out, int K, int N, int group_size, w4a16_dtype dtype,
                            cudaStream_t stream) {
@@ -192,8 +248,8 @@ w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales, const ui
   w4a16_status st = check_int4_shape(0, N, K, group_size);
   if (st != W4A16_OK) return st;
   if (N == 0) return W4A16_OK;
-  if (!ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(qzeros) || !ok_ptr(W_out)) return W4A16_ERR_INVALID_ARG;
-  if (g_idx && !aligned16(g_idx)) return W4A16_ERR_INVALID_ARG;
+  if (!ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(W_out)) return W4A16_ERR_INVALID_ARG;
+  if ((qzeros && !aligned16(qzeros)) || (g_idx && !aligned16(g_idx))) return W4A16_ERR_INVALID_ARG;
   return from_cuda(launch_dequant_int4(qweight, static_cast<const uint16_t*>(scales), qzeros, g_idx,
                                        static_cast<uint16_t*>(W_out), K, N, group_size, dtype == W4A16_BF16,
                                        stream));
@@ -216,7 +272,9 @@ w4a16_status w4a16_quantize(const float* W, int K, int N, int group_size, uint32
   w4a16_status st = check_int4_shape(0, N, K, group_size);
   if (st != W4A16_OK) return st;
   if (N == 0) return W4A16_OK;
-  if (!ok_ptr(W) || !ok_ptr(qweight) || !ok_ptr(scales) || !ok_ptr(qzeros)) return W4A16_ERR_INVALID_ARG;
+  // qzeros NULL: symmetric quantization (no zero points stored)
+  if (!ok_ptr(W) || !ok_ptr(qweight) || !ok_ptr(scales) || (qzeros && !aligned16(qzeros)))
+    return W4A16_ERR_INVALID_ARG;
   return from_cuda(
       launch_quantize_rtn(W, K, N, group_size, qweight, static_cast<uint16_t*>(scales), qzeros, stream));
 }

@@ -239,16 +239,29 @@ __device__ __forceinline__ DqConstBF16Fma dq_const_bf16_fma(uint32_t z, uint32_t
   return c;
 }
 
+// fma(half H of p, low half of s, zs) with fp16 operands and an fp32 sum
+template <int H>
+__device__ __forceinline__ float fma_f16_f32(uint32_t p, uint32_t s, float zs) {
+  float d;
+  if (H == 0)
+    asm("{\n\t.reg .f16 a0, a1, s0, s1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {s0, s1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, s0, %3;\n\t}"
+        : "=f"(d)
+        : "r"(p), "r"(s), "f"(zs));
+  else
+    asm("{\n\t.reg .f16 a0, a1, s0, s1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {s0, s1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a1, s0, %3;\n\t}"
+        : "=f"(d)
+        : "r"(p), "r"(s), "f"(zs));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t dq_pair_bf16_fma(uint32_t p, float zs, uint32_t s) {
-  float lo, hi;
-  asm("{\n\t.reg .f16 a0, a1, s0, s1;\n\t"
-      "mov.b32 {a0, a1}, %2;\n\t"
-      "mov.b32 {s0, s1}, %3;\n\t"
-      "fma.rn.f32.f16 %0, a0, s0, %4;\n\t"
-      "fma.rn.f32.f16 %1, a1, s0, %4;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(p), "r"(s), "f"(zs));
-  return pack2_rn(lo, hi, true);
+  return pack2_rn(fma_f16_f32<0>(p, s, zs), fma_f16_f32<1>(p, s, zs), true);
 }
 
 __device__ __forceinline__ void dq_word_bf16_fma(uint32_t w, const DqConstBF16Fma& c, uint32_t out[4]) {
@@ -278,6 +291,22 @@ __device__ __forceinline__ void dq_word_nat_f16(uint32_t w, uint32_t zmix, uint3
     const uint32_t u = prmt(w, 0u, 0x1111u * j);
     out[j] = hmul2_f16(hsub2_f16(lop3_and_or(u, 0x00F0000Fu, 0x54006400u), zmix), s2);
   }
+}
+
+// The FMA route in natural K order costs no more than in the (j, j + 4)
+// order: each FMA yields its own fp32 value and the conversion pairs any two,
+// so pair (2j, 2j + 1) takes its codes from two magic registers, the
+// 1024 + q one (rows 0, 4 / 2, 6) and the 64 + q one (rows 1, 5 / 3, 7).
+__device__ __forceinline__ void dq_word_nat_bf16_fma(uint32_t w, const DqConstBF16Fma& c, uint32_t out[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t p04 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+  const uint32_t p15 = lop3_and_or(w, 0x00F000F0u, 0x54005400u);
+  const uint32_t p26 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);
+  const uint32_t p37 = lop3_and_or(w8, 0x00F000F0u, 0x54005400u);
+  out[0] = pack2_rn(fma_f16_f32<0>(p04, c.s, c.z_lo), fma_f16_f32<0>(p15, c.s, c.z_hi), true);
+  out[1] = pack2_rn(fma_f16_f32<0>(p26, c.s, c.z_lo), fma_f16_f32<0>(p37, c.s, c.z_hi), true);
+  out[2] = pack2_rn(fma_f16_f32<1>(p04, c.s, c.z_lo), fma_f16_f32<1>(p15, c.s, c.z_hi), true);
+  out[3] = pack2_rn(fma_f16_f32<1>(p26, c.s, c.z_lo), fma_f16_f32<1>(p37, c.s, c.z_hi), true);
 }
 
 __device__ __forceinline__ void dq_word_nat_bf16(uint32_t w, const DqConstBF16& c, uint32_t out[4]) {

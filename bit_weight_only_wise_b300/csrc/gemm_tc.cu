@@ -99,8 +99,14 @@ struct GemmParams {
   int kb_per_split;
   const int32_t* g_idx;
   const uint16_t* scales;
-  const uint32_t* qz;
+  const uint32_t* qz;     // nullptr: symmetric (every zero point 8)
+  int gsize;              // rows per group
+  int NG;                 // groups along K
+  uint32_t gmagic;        // ceil(2^31 / (gsize / 32)), one group: 2^31 >> 14 (see fetch)
   const float* absmax;
+  const uint8_t* absmax_q;  // NF4 double quantization: codes, or nullptr
+  const float* absmax_s2;   // NF4 double quantization: second-level scales [K/64][nc2]
+  int nc2;
   const float* codebook;  // device table, or nullptr: cb_builtin
   Cb16 cb_builtin;
   uint16_t* Y;
@@ -155,13 +161,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (FMT == kFmtNF4 && threadIdx.x < 16) bars->cb[threadIdx.x] = p.codebook ? p.codebook[threadIdx.x] : p.cb_builtin.v[threadIdx.x];
   if (FMT == kFmtInt4Act) {
-    const int G = p.K / 128;
+    const int G = p.NG;
     for (int i = threadIdx.x; i < G * kBN; i += kThreads) {
       const int g = i / kBN, c = i % kBN, n = n0 + c;
       uint32_t v = 0;
       if (n < p.N) {
         const uint32_t sb = p.scales[(size_t)g * p.N + n];
-        const uint32_t z = (p.qz[(size_t)g * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu;
+        const uint32_t z = p.qz ? (p.qz[(size_t)g * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu : 8u;
         v = sb | (z << 16);
       }
       act_tab[i] = v;
@@ -234,9 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fetch = [&](int kb, uint32_t& s_out, uint32_t& z_out, float& am_out) {  // kb: absolute K block
       if (!ok || kb >= kb0 + nkb || FMT == kFmtInt4Act) return;
       if (FMT == kFmtInt4) {
-        const int grp = kb >> 1;  // 128-row groups, 64-row stages
+        // this thread's 32 rows of the 64-row block lie in one group (groups
+        // of 32, 64, any multiple of 128, or one group for all of K): the
+        // group of 32-row chunk 2 kb + h is floor(chunk / (g / 32)), taken as
+        // a multiply-high by the host's gmagic = ceil(2^31 / (g / 32)), exact
+        // for every chunk index below 2^14 and divisor up to 2^14
+        const int grp = (int)__umulhi((uint32_t)(2 * (2 * kb + h)), p.gmagic);
+        if (grp >= p.NG) {  // rows past K (a last block shorter than 64 rows): X is zero there
+          s_out = z_out = 0;
+          return;
+        }
         s_out = p.scales[(size_t)grp * p.N + n];
-        z_out = (p.qz[(size_t)grp * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu;
+        z_out = p.qz ? (p.qz[(size_t)grp * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu : 8u;
+      } else if (p.absmax_q) {  // double quantization: absmax_hat = fl32(code * s2)
+        am_out = __fmul_rn((float)p.absmax_q[(size_t)kb * p.N + n], p.absmax_s2[(size_t)kb * p.nc2 + (n >> 8)]);
       } else {
         am_out = p.absmax[(size_t)kb * p.N + n];  // 64-row blocks == stages
       }
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fetch(kb0 + grp + kStep, s_nxt, z_nxt, am_nxt);
     fetch(kb0 + grp + 2 * kStep, s_nx2, z_nx2, am_nx2);
     uint32_t zmix = dq_zmix_f16(z_raw), s2 = s_raw * 0x10001u;
-    DqConstBF16 cbf = dq_const_bf16(z_raw, s_raw);
+    DqConstBF16Fma cbf = dq_const_bf16_fma(z_raw, s_raw);
 
     bool alive = true;
     for (int it = grp; it < nkb && alive; it += kDqGroups) {
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         am_nxt = am_nx2;
         fetch(kb0 + it + 2 * kStep, s_nx2, z_nx2, am_nx2);
         if (FMT == kFmtInt4) {
-          if (BF16) cbf = dq_const_bf16(z_raw, s_raw);
+          if (BF16) cbf = dq_const_bf16_fma(z_raw, s_raw);
           else {
             zmix = dq_zmix_f16(z_raw);
             s2 = s_raw * 0x10001u;
@@ -287,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kWords; ++i) {
           const int4 ga = __ldg(gp + 2 * i), gb = __ldg(gp + 2 * i + 1);
-          const int G = p.K / 128;
+          const int G = p.NG;
           const int gr[8] = {checked_group(ga.x, G, p.dev_status), checked_group(ga.y, G, p.dev_status),
                              checked_group(ga.z, G, p.dev_status), checked_group(ga.w, G, p.dev_status),
                              checked_group(gb.x, G, p.dev_status), checked_group(gb.y, G, p.dev_status),
@@ -313,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kWords; ++i) {
           uint32_t* o = regs + 4 * i;
           if (FMT == kFmtNF4) dq_word_nat_nf4<BF16>(wv[i], bars->cb, am, o);
-          else if (BF16) dq_word_nat_bf16(wv[i], cbf, o);
+          else if (BF16) dq_word_nat_bf16_fma(wv[i], cbf, o);
           else dq_word_nat_f16(wv[i], zmix, s2, o);
         }
       }
@@ -424,7 +441,7 @@ cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const Gemm
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(dev_bit, std::memory_order_release);
   }
-  const int smem = smem_fixed<FMT>() + (FMT == kFmtInt4Act ? (p.K / 128) * kActTableRowBytes : 0);
+  const int smem = smem_fixed<FMT>() + (FMT == kFmtInt4Act ? p.NG * kActTableRowBytes : 0);
   if (smem > kMaxSmem) return cudaErrorInvalidValue;
   gemm_tc_kernel<FMT, BF16><<<grid, kThreads, smem, st>>>(tmX, tmW, p);
   return cudaGetLastError();
@@ -459,13 +476,13 @@ int gemm_tokens_per_cta(int M, bool act_order) {
   return (M + 31) / 32 * 32;
 }
 
-bool gemm_act_order_fits(int K) {
-  return smem_fixed<kFmtInt4Act>() + (K / 128) * kActTableRowBytes <= kMaxSmem;
+bool gemm_act_order_fits(int NG) {
+  return smem_fixed<kFmtInt4Act>() + NG * kActTableRowBytes <= kMaxSmem;
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st) {
   const bool act = a.g_idx != nullptr;
-  if (act && (nf4 || !gemm_act_order_fits(a.K))) return cudaErrorInvalidValue;
+  if (act && (nf4 || !gemm_act_order_fits(a.NG))) return cudaErrorInvalidValue;
   const int BT = gemm_tokens_per_cta(a.M, act);
   CUtensorMap tmX, tmW;
   const CUtensorMapDataType xdt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -479,6 +496,18 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   p.g_idx = a.g_idx;
   p.scales = a.scales;
   p.qz = a.qz;
+  p.gsize = a.gsize;
+  p.NG = a.NG;
+  {
+    // 32-row chunks per group; a single group (including g = K not a multiple
+    // of 32) uses the largest divisor, 2^14, which every chunk index is below
+    uint32_t d = (a.NG <= 1 || a.gsize % 32) ? (1u << 14) : (uint32_t)(a.gsize / 32);
+    if (d > (1u << 14)) d = 1u << 14;
+    p.gmagic = (uint32_t)(((1ull << 31) + d - 1) / d);
+  }
+  p.absmax_q = a.absmax_q;
+  p.absmax_s2 = a.absmax_s2;
+  p.nc2 = (a.N + 255) / 256;
   p.absmax = a.absmax;
   p.codebook = a.codebook;
   p.cb_builtin = a.cb_builtin;

@@ -1,9 +1,10 @@
 // Split-K weight-streaming kernel for act-order decode shapes (1 <= M <= 16,
-// g_idx as stored: every K row may belong to a different group).  Plain groups
-// and NF4 run on the warp-specialized kernel (gemv_ws.cu); this one serves the
-// stored act-order layout, where each packed word needs the (scale, zero) of
-// eight different groups, gathered from global memory per row.  For speed,
-// prepack act-order checkpoints once (act_order.cu) and use the plain kernels.
+// g_idx as stored: every K row may belong to a different group) with more
+// groups than the warp-specialized kernel's shared-memory table holds (that
+// kernel, gemv_ws.cu, serves every other decode format).  Each packed word
+// needs the (scale, zero) of eight different groups, gathered here from
+// global memory per row.  For speed, prepack act-order checkpoints once
+// (act_order.cu) and use the plain kernels.
 //
 // Y[M,N] = X[M,K] . W_hat[K,N] ("GPTQ与bitsandbytes对比：谁是2024年大模型量化的终极选择？",
 // GPTQ section, --act-order).
@@ -80,15 +81,16 @@ struct Dq<kInt4Act, BF16> {
     if (ok) {
       const int4 g0 = __ldg(reinterpret_cast<const int4*>(a.g_idx + row0));
       const int4 g1 = __ldg(reinterpret_cast<const int4*>(a.g_idx + row0 + 4));
-      const int gr[8] = {checked_group(g0.x, a.G, a.dev_status), checked_group(g0.y, a.G, a.dev_status),
-                         checked_group(g0.z, a.G, a.dev_status), checked_group(g0.w, a.G, a.dev_status),
-                         checked_group(g1.x, a.G, a.dev_status), checked_group(g1.y, a.G, a.dev_status),
-                         checked_group(g1.z, a.G, a.dev_status), checked_group(g1.w, a.G, a.dev_status)};
+      const int gr[8] = {checked_group(g0.x, a.NG, a.dev_status), checked_group(g0.y, a.NG, a.dev_status),
+                         checked_group(g0.z, a.NG, a.dev_status), checked_group(g0.w, a.NG, a.dev_status),
+                         checked_group(g1.x, a.NG, a.dev_status), checked_group(g1.y, a.NG, a.dev_status),
+                         checked_group(g1.z, a.NG, a.dev_status), checked_group(g1.w, a.NG, a.dev_status)};
       const int col = col0 + c4;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         s[r] = __ldg(a.scales + (size_t)gr[r] * a.N + col);
-        z[r] = (__ldg(a.qz + (size_t)gr[r] * (a.N >> 3) + (col >> 3)) >> (4 * (col & 7))) & 0xFu;
+        // symmetric weights (no zero points): every zero point is 8
+        z[r] = a.qz ? (__ldg(a.qz + (size_t)gr[r] * (a.N >> 3) + (col >> 3)) >> (4 * (col & 7))) & 0xFu : 8u;
       }
     } else {
 #pragma unroll
@@ -125,11 +127,11 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   uint64_t* bar = full[warp];
   volatile int abort_flag = 0;  // per-warp pipeline: nobody else raises it
 
-  const Range R{(long long)a.blocks_n * a.G, (int)gridDim.x};
+  const Range R{(long long)a.blocks_n * a.KB, (int)gridDim.x};
   const int cta = blockIdx.x;
   const long long u0 = R.start(cta);
   const int nu = (int)(R.start(cta + 1) - u0);
-  const int first_block = (int)(u0 / a.G);
+  const int first_block = (int)(u0 / a.KB);
 
   Dq<FMT, BF16> dq;
   dq.tab = s_tab[warp];
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
 
   // lane 0 streams this warp's slice of the CTA's units, kRing ahead: (tx, ty)
   // is the TMA coordinate of the next unit to copy, is_ its stage
-  int tx = first_block * kGemvCols + warp * 32, ty = (int)(u0 % a.G) * 16, is_ = 0;
-  const int ty_end = a.G * 16;
+  int tx = first_block * kGemvCols + warp * 32, ty = (int)(u0 % a.KB) * 16, is_ = 0;
+  const int ty_end = a.KB * 16;
   auto advance = [&]() {
     is_ = (is_ + 1 == kRing) ? 0 : is_ + 1;
     ty += 16;
@@ -157,24 +159,26 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
     tma_load_2d(ring + is_ * kStage + kTileBytes, &tmX, &bar[is_], ty * 8, 0);
     advance();
   };
-  // The packed weights do not depend on the previous kernel in the stream, so
-  // the first stages' weight copies start before waiting for it; activations
-  // and the workspace are touched only after griddep_wait.
-  int first_ty[kRing];
+  // Nothing the caller owns is read into shared memory before griddep_wait
+  // (the kernel before this one may still be writing it); until then the
+  // first stages' weights are only prefetched into L2.
   const int n_first = nu < kRing ? nu : kRing;
   if (lane == 0) {
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmX);
+    int px = tx, py = ty;
     for (int k = 0; k < n_first; ++k) {
-      first_ty[k] = ty;
-      mbar_arrive_expect_tx(&bar[is_], kStage);
-      tma_load_2d(ring + is_ * kStage, &tmW, &bar[is_], tx, ty);
-      advance();
+      tma_prefetch_l2_2d(&tmW, px, py);
+      py += 16;
+      if (py == ty_end) {
+        py = 0;
+        px += kGemvCols;
+      }
     }
   }
   griddep_wait();
   if (lane == 0)
-    for (int k = 0; k < n_first; ++k) tma_load_2d(ring + k * kStage + kTileBytes, &tmX, &bar[k], first_ty[k] * 8, 0);
+    for (int k = 0; k < n_first; ++k) issue();
   griddep_launch_dependents();
 
   float acc[NT][2][4];
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
   const uint32_t ring_s = smem_u32(ring);
 
   int cur_b = -1;
-  int b = first_block, g = (int)(u0 % a.G);  // current unit
+  int b = first_block, g = (int)(u0 % a.KB);  // current unit
   int s = 0;
   uint32_t phase = 0;
   if (nu > 0) dq.fetch(a, g, b * kGemvCols + warp * 32, lane);
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
     __syncwarp();
     dq.begin(gl);
     int bn = b, gn = g + 1;  // next unit
-    if (gn == a.G) {
+    if (gn == a.KB) {
       gn = 0;
       ++bn;
     }
@@ -355,8 +359,11 @@ cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st) {
-  // plain groups: the warp-specialized kernel (gemv_ws.cu); act-order: this one
-  return a.g_idx ? launch_gemv<kInt4Act>(a, bf16, st) : launch_gemv_ws_int4(a, bf16, st);
+  // grouped weights: the warp-specialized kernel (gemv_ws.cu); act-order: the
+  // same kernel with its shared-memory table when every group fits, else this
+  // one (global-memory lookups)
+  if (!a.g_idx) return launch_gemv_ws_int4(a, bf16, st);
+  return gemv_ws_act_fits(a.NG) ? launch_gemv_ws_act(a, bf16, st) : launch_gemv<kInt4Act>(a, bf16, st);
 }
 
 // NF4 runs on the warp-specialized kernel as well (gemv_ws.cu)
@@ -365,8 +372,8 @@ cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st) { ret
 GemvPlan gemv_plan(int M, int N, int K, int fmt) {
   GemvPlan p{};
   p.blocks_n = (N + kGemvCols - 1) / kGemvCols;
-  p.G = (K + 127) / 128;
-  const long long U = (long long)p.blocks_n * p.G;
+  p.KB = (K + 127) / 128;
+  const long long U = (long long)p.blocks_n * p.KB;
   // at least kMinUnits units (64 KB of weights) per CTA: below that the
   // per-CTA start-up and the split reduction cost more than the bytes
   constexpr long long kMinUnits = 4;

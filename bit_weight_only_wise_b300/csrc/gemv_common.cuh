@@ -69,8 +69,8 @@ __device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, i
                                             int lane, int b, const float (&acc)[NT][2][4]) {
   const int gl = lane >> 2, c = lane & 3;
   const int col0 = b * kGemvCols + warp * 32 + 4 * gl;
-  const int i_first = R.owner((long long)b * a.G);
-  const int i_last = R.owner((long long)(b + 1) * a.G - 1);
+  const int i_first = R.owner((long long)b * a.KB);
+  const int i_last = R.owner((long long)(b + 1) * a.KB - 1);
   if (i_first == i_last) {
     if (col0 >= a.N) return false;
 #pragma unroll
@@ -111,9 +111,9 @@ template <int NT, bool BF16>
 __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, int warp, int lane, int b) {
   const int col = b * kGemvCols + warp * 32 + lane;
   if (col >= a.N) return;
-  const int i_first = R.owner((long long)b * a.G);
-  const int i_last = R.owner((long long)(b + 1) * a.G - 1);
-  const int sg_first = R.start(i_first) == (long long)b * a.G ? 0 : 1;
+  const int i_first = R.owner((long long)b * a.KB);
+  const int i_last = R.owner((long long)(b + 1) * a.KB - 1);
+  const int sg_first = R.start(i_first) == (long long)b * a.KB ? 0 : 1;
   const size_t stride = (size_t)a.M * 32;  // floats per slice slot
   auto slot = [&](int i) -> const float* {
     return a.partial + ((size_t)(i * 2 + (i == i_first ? sg_first : 0)) * kSliceWarps + warp) * stride + lane;
@@ -162,9 +162,9 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
   const int bs[2] = {b0, b1};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    first[h] = R.owner((long long)bs[h] * a.G);
-    last[h] = R.owner((long long)(bs[h] + 1) * a.G - 1);
-    sgf[h] = R.start(first[h]) == (long long)bs[h] * a.G ? 0 : 1;
+    first[h] = R.owner((long long)bs[h] * a.KB);
+    last[h] = R.owner((long long)(bs[h] + 1) * a.KB - 1);
+    sgf[h] = R.start(first[h]) == (long long)bs[h] * a.KB ? 0 : 1;
     col[h] = bs[h] * kGemvCols + warp * 32 + lane;
   }
   float sum[2] = {0.f, 0.f};
@@ -204,11 +204,11 @@ __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R,
   if (lane == 0) {
     __threadfence();
     if (p0 >= 0) {
-      const uint32_t w = (uint32_t)(R.owner((long long)(p0 + 1) * a.G - 1) - R.owner((long long)p0 * a.G));
+      const uint32_t w = (uint32_t)(R.owner((long long)(p0 + 1) * a.KB - 1) - R.owner((long long)p0 * a.KB));
       last0 = sm100::ticket_inc_acquire(a.counters + p0 * kSliceWarps + warp, w) == w;
     }
     if (p1 >= 0) {
-      const uint32_t w = (uint32_t)(R.owner((long long)(p1 + 1) * a.G - 1) - R.owner((long long)p1 * a.G));
+      const uint32_t w = (uint32_t)(R.owner((long long)(p1 + 1) * a.KB - 1) - R.owner((long long)p1 * a.KB));
       last1 = sm100::ticket_inc_acquire(a.counters + p1 * kSliceWarps + warp, w) == w;
     }
   }

@@ -63,11 +63,12 @@ extern "C" w4a16_status w4a16_gemv_noalloc(const void* X, const uint32_t* qweigh
   if (M < 0 || N < 0 || K <= 0 || M > W4A16_MAX_M || N > W4A16_MAX_N || K > W4A16_MAX_K)
     return W4A16_ERR_INVALID_ARG;
   if (N % 8 || K % 8 || group_size <= 0 || K % group_size) return W4A16_ERR_INVALID_ARG;
-  if (group_size != 128) return W4A16_ERR_UNSUPPORTED;
+  if (!w4a16::int4_group_supported(K, group_size)) return W4A16_ERR_UNSUPPORTED;
   if (M > W4A16_GEMV_MAX_M) return W4A16_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return W4A16_OK;
   auto ok16 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (!ok16(X) || !ok16(qweight) || !ok16(scales) || !ok16(qzeros) || !ok16(Y)) return W4A16_ERR_INVALID_ARG;
+  if (!ok16(X) || !ok16(qweight) || !ok16(scales) || !ok16(Y)) return W4A16_ERR_INVALID_ARG;
+  if (qzeros && (reinterpret_cast<uintptr_t>(qzeros) & 15u)) return W4A16_ERR_INVALID_ARG;  // NULL: symmetric
   if (g_idx && (reinterpret_cast<uintptr_t>(g_idx) & 15u)) return W4A16_ERR_INVALID_ARG;
   const size_t need = w4a16_workspace_bytes(M, N, K);
   if (need > (size_t)W4A16_NOALLOC_SCRATCH_BYTES) return W4A16_ERR_UNSUPPORTED;

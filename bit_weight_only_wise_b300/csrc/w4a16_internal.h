@@ -23,7 +23,11 @@ const Cb16& nf4_builtin_codebook();
 // ----------------------------------------------------------- split-K GEMV
 constexpr int kGemvThreads = 256;            // 8 warps, one 32-column slice each
 constexpr int kGemvCols = 256;               // columns per unit
-enum GemvFmt { kInt4 = 0, kInt4Act = 1, kNF4 = 2 };
+// kInt4: grouped scales and zero points (any supported group size, symmetric
+// or not); kInt4Act: the same with an act-order map; kNF4: fp32 absmax;
+// kNF4DQ: NF4 with double-quantized absmax (8-bit codes and a second-level
+// fp32 scale)
+enum GemvFmt { kInt4 = 0, kInt4Act = 1, kNF4 = 2, kNF4DQ = 3 };
 // persistent grid: CTAs resident per SM, by token tiles (M <= 8: one tile of
 // 8 tokens) and format (register and shared-memory budget of each variant)
 constexpr int kGemvMaxCTAsPerSM = 3;
@@ -37,7 +41,7 @@ constexpr size_t kCountersBytes = (size_t)kMaxColBlocks * (kGemvCols / 32) * siz
 
 struct GemvPlan {
   int blocks_n;  // 256-column blocks
-  int G;         // 128-row K groups
+  int KB;        // 128-row blocks along K (units per column block)
   int ctas;      // persistent grid size
   size_t workspace_bytes;
 };
@@ -47,36 +51,58 @@ GemvPlan gemv_plan(int M, int N, int K, int fmt);
 struct GemvArgs {
   const uint16_t* X;
   const uint32_t* qw;
-  const uint16_t* scales;  // INT4: fp16 scales
-  const uint32_t* qz;      // INT4 packed zeros
-  const int32_t* g_idx;    // INT4 act-order map or nullptr
-  const float* absmax;     // NF4
-  const float* codebook;   // NF4 table in device memory, or nullptr: cb_builtin
-  Cb16 cb_builtin;         // NF4 table used when codebook is nullptr
+  const uint16_t* scales;   // INT4: fp16 scales [NG, N]
+  const uint32_t* qz;       // INT4 packed zeros [NG, N/8], or nullptr: symmetric (every zero point 8)
+  const int32_t* g_idx;     // INT4 act-order map or nullptr
+  const float* absmax;      // NF4: fp32 [K/64, N]
+  const uint8_t* absmax_q;  // NF4 double quantization: 8-bit codes [K/64, N]
+  const float* absmax_s2;   // NF4 double quantization: fp32 [K/64, ceil(N/256)]
+  const float* codebook;    // NF4 table in device memory, or nullptr: cb_builtin
+  Cb16 cb_builtin;          // NF4 table used when codebook is nullptr
   uint16_t* Y;
   float* partial;
   int* counters;
   int* dev_status;
   int M, N, K;
-  int G;         // 128-row K groups
-  int blocks_n;  // 256-column blocks
+  int KB;          // 128-row blocks along K (units per column block)
+  int NG;          // scale groups along K
+  int gsize;       // rows per group (INT4)
+  int kbpg;        // 128-row units per group (set by the launcher)
+  int nwz;         // zero words per row to copy: N / 8, or 0 for symmetric weights (launcher)
+  uint32_t zxor;   // 0, or 0x88888888 for symmetric weights: zero points of 8 (launcher)
+  int blocks_n;    // 256-column blocks
   int ctas;
+  int stages;      // pipeline depth (set by the launcher)
+  int tab_stride;  // act-order: bytes per group in the shared-memory table (set by the launcher)
 };
 
 cudaError_t launch_gemv_int4(const GemvArgs& a, bool bf16, cudaStream_t st);
-// plain-group INT4 and NF4 decode on the warp-specialized kernel
+// the warp-specialized decode kernel: grouped INT4 (any supported group
+// size, symmetric or not), act-order through a shared-memory table of the
+// column block's scales and zeros (when it fits: gemv_ws_act_fits), NF4
 cudaError_t launch_gemv_ws_int4(const GemvArgs& a, bool bf16, cudaStream_t st);
+cudaError_t launch_gemv_ws_act(const GemvArgs& a, bool bf16, cudaStream_t st);
+bool gemv_ws_act_fits(int NG);
 cudaError_t launch_gemv_ws_nf4(const GemvArgs& a, bool bf16, cudaStream_t st);
 cudaError_t launch_gemv_nf4(const GemvArgs& a, bool bf16, cudaStream_t st);
+// Group sizes the decode kernel supports: 32 and 64 (several groups per
+// 128-row unit), multiples of 128, and a single group (per-channel, g = K).
+inline bool int4_group_supported(int K, int g) {
+  return g == 32 || g == 64 || g % 128 == 0 || g == K;
+}
 
 // ------------------------------------------------------ tensor-core GEMM
 struct GemmArgs {
   const void* X;
   const uint32_t* qw;
   const uint16_t* scales;  // INT4
-  const uint32_t* qz;      // INT4
+  const uint32_t* qz;      // INT4, or nullptr: symmetric (every zero point 8)
   const int32_t* g_idx;    // INT4 act-order map or nullptr
+  int gsize;               // INT4 rows per group
+  int NG;                  // INT4 groups along K
   const float* absmax;     // NF4
+  const uint8_t* absmax_q; // NF4 double quantization: 8-bit codes [K/64, N], or nullptr
+  const float* absmax_s2;  // NF4 double quantization: fp32 [K/64, ceil(N/256)]
   const float* codebook;   // NF4 table in device memory, or nullptr: cb_builtin
   Cb16 cb_builtin;
   uint16_t* Y;
@@ -97,8 +123,8 @@ struct GemmSplit {
   size_t workspace_bytes;  // 0 when not split
 };
 GemmSplit gemm_split_plan(int M, int N, int K, bool act_order);
-// Whether the act-order variant's per-CTA (scale, zero) table fits for this K.
-bool gemm_act_order_fits(int K);
+// Whether the act-order variant's per-CTA (scale, zero) table fits for NG groups.
+bool gemm_act_order_fits(int NG);
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t st);
 
 // ------------------------------------------------- per-device kernel setup
@@ -126,6 +152,11 @@ cudaError_t launch_dequant_int4(const uint32_t* qw, const uint16_t* scales, cons
 // codebook: a device table, or nullptr for the built-in one
 cudaError_t launch_dequant_nf4(const uint32_t* qw, const float* absmax, const float* codebook, uint16_t* out,
                                int K, int N, int blocksize, bool bf16, cudaStream_t st);
+cudaError_t launch_dequant_nf4dq(const uint32_t* qw, const uint8_t* absmax_q, const float* absmax_s2,
+                                 const float* codebook, uint16_t* out, int K, int N, int blocksize, bool bf16,
+                                 cudaStream_t st);
+cudaError_t launch_double_quantize(const float* absmax, int rows, int N, uint8_t* absmax_q, float* absmax_s2,
+                                   cudaStream_t st);
 cudaError_t launch_quantize_rtn(const float* W, int K, int N, int group_size, uint32_t* qw, uint16_t* scales,
                                 uint32_t* qz, cudaStream_t st);
 cudaError_t launch_quantize_nf4(const float* W, int K, int N, int blocksize, const float* codebook, uint32_t* qw,

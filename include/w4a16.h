@@ -5,21 +5,31 @@
  *
  * Two weight formats:
  *
- *  INT4 (GPTQ / AWQ checkpoints).  Asymmetric round-to-nearest quantization
- *    with one fp16 scale and one 4-bit zero point per group of 128 rows along
- *    K (cloud.tencent.com/developer/article/2726413 §2.1 asymmetric
+ *  INT4 (GPTQ / AWQ checkpoints).  Round-to-nearest quantization with one
+ *    fp16 scale and one 4-bit zero point per group of group_size rows along K
+ *    (cloud.tencent.com/developer/article/2726413 §2.1 asymmetric
  *    quantization stores a zero point; §2.2 group-wise granularity, e.g. 128
- *    elements per scale; "模型量化实践：GPTQ 与 AWQ 在生产环境的精度与速度权衡"
- *    §3.1 bits=4, group_size=128, zero_point=True).  An optional act-order map
- *    g_idx assigns every K row to its group ("GPTQ与bitsandbytes对比" GPTQ
- *    section, --act-order; same §3.1, desc_act=True).
- *      W_hat[k,n] = RNE_dtype((q[k,n] - z[g,n]) * s[g,n]),  g = g_idx[k] or k/128
+ *    elements per scale, or one per channel; "模型量化实践：GPTQ 与 AWQ 在生产
+ *    环境的精度与速度权衡" §3.1 bits=4, group_size=128, zero_point=True;
+ *    "GPTQ、AWQ与Bitsandbytes" §3.1 node 3: groups of 128, 64 or 32).
+ *    group_size: 32, 64, any multiple of 128, or K (one group per column).
+ *    Symmetric weights (same §2.1: zero point fixed at 0) are passed with
+ *    qzeros == NULL: their signed codes are stored as code + 8, i.e. every
+ *    zero point is 8.  An optional act-order map g_idx assigns every K row to
+ *    its group ("GPTQ与bitsandbytes对比" GPTQ section, --act-order; "模型量化
+ *    实践" §3.1, desc_act=True).
+ *      W_hat[k,n] = RNE_dtype((q[k,n] - z[g,n]) * s[g,n]),
+ *      g = g_idx[k] or k / group_size,  z = 8 when qzeros is NULL
  *
  *  NF4 (bitsandbytes).  Codes index a 16-entry normal-float codebook, scaled
  *    per block of 64 consecutive K rows by an fp32 absmax ("LLM量化技术深度对比:
  *    GPTQ vs AWQ vs bitsandbytes 2026基准全解析" key-data item 2; "GPTQ、AWQ与
  *    Bitsandbytes：大模型量化三大技术路径深度对比" §2.3 block-wise NF4).
  *      W_hat[k,n] = RNE_dtype(fl32(C[q[k,n]] * absmax[k/64, n]))
+ *    With double quantization ("GPTQ、AWQ与Bitsandbytes" §3.3
+ *    use_double_quant; §4.3: a scale of the scale is stored) absmax is held
+ *    as 8-bit codes with one fp32 second-level scale per 256 consecutive
+ *    columns of an absmax row:  absmax = fl32(code * s2)  (nf4dq_* calls).
  *
  * Fusing the dequantization into the product -- never writing 16-bit weights
  * to memory -- is what makes the format fast ("LLM量化技术深度对比" key-data
@@ -31,11 +41,14 @@
  *   Y       [M, N]     same dtype as X
  *   qweight uint32 [K/8, N]: code of row 8i+j, column n in bits 4j..4j+3 of
  *                      word [i, n] (8 codes per word, packed along K)
- *   scales  fp16 [K/128, N]                 (INT4)
- *   qzeros  uint32 [K/128, N/8]: zero point of column 8c+j in bits 4j.. of
- *                      word [g, c] (packed along N; the stored value is z)
- *   g_idx   int32 [K]  row -> group, each value in [0, K/128); NULL means k/128
+ *   scales  fp16 [G, N], G = K / group_size  (INT4)
+ *   qzeros  uint32 [G, N/8]: zero point of column 8c+j in bits 4j.. of
+ *                      word [g, c] (packed along N; the stored value is z);
+ *                      NULL: symmetric weights (every zero point 8)
+ *   g_idx   int32 [K]  row -> group, each value in [0, G); NULL means k/group_size
  *   absmax  fp32 [K/64, N]                  (NF4)
+ *   absmax_q  uint8 [K/64, N], absmax_s2 fp32 [K/64, ceil(N/256)]
+ *                      (NF4 with double-quantized absmax)
  *   codebook16 fp32 [16], ascending         (NF4; NULL = the built-in table,
  *                      see nf4_default_codebook)
  *
@@ -52,14 +65,12 @@
  *    0 < K <= W4A16_MAX_K; outside them W4A16_ERR_INVALID_ARG, nothing
  *    launched.
  *  - M == 0 or N == 0 is a valid empty problem: W4A16_OK, nothing launched.
- *  - The product kernels are launched as programmatic dependents of the
- *    kernel before them on `stream`: they start copying qweight, scales,
- *    qzeros, absmax and the codebook while that kernel may still be running,
- *    and touch X, g_idx / perm, Y and the workspace only after it has
- *    completed.  A kernel that writes the weights directly before a call
- *    must therefore not signal early completion
- *    (cudaTriggerProgrammaticLaunchCompletion) before those writes; an
- *    ordinary kernel, a copy or an event between the two needs nothing.
+ *  - The decode kernels are launched as programmatic dependents of the
+ *    kernel before them on `stream`, so their start overlaps its end.  Until
+ *    that kernel has completed they only prefetch weight lines into L2 (the
+ *    device's point of coherence, so a prefetch cannot return stale data);
+ *    every read of a caller's buffer happens after it.  Callers need no
+ *    ordering beyond the stream's.
  *  - The dtype of X and Y is `dtype`; scales are always fp16, absmax fp32.
  */
 #ifndef W4A16_H
@@ -99,7 +110,13 @@ typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
  * runs the split-K decode kernel (as w4a16_gemv), larger M the tcgen05
  * tensor-core kernel, which also splits K when its output tiles alone would
  * leave SMs idle (fp32 partial tiles summed in a fixed order: deterministic).
- *   group_size: 128.
+ *   group_size: 32, 64, a multiple of 128, or K; others W4A16_ERR_UNSUPPORTED.
+ *   qzeros: NULL for symmetric weights.
+ *   g_idx with M > 16: the tensor-core kernel keeps every group's (scale,
+ *     zero) of its 128 columns in shared memory, which holds at most 290
+ *     groups (K <= 37120 at group_size 128); beyond that the call returns
+ *     W4A16_ERR_UNSUPPORTED -- prepack such checkpoints
+ *     (w4a16_act_order_prepack).
  *   workspace: device scratch of at least w4a16_workspace_bytes(M, N, K)
  *     bytes, zero-filled by the caller before its first use.  Its first part
  *     holds the split-K tickets, which every call that completes leaves at
@@ -137,7 +154,7 @@ w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absma
                       int* dev_status, cudaStream_t stream);
 
 /* W_out[K, N] (dtype) = W_hat, the INT4 dequantization written out; bit-exact
- * with the definition above.  g_idx may be NULL. */
+ * with the definition above.  g_idx may be NULL; qzeros NULL: symmetric. */
 w4a16_status w4a16_dequant(const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
                            const int32_t* g_idx, void* W_out, int K, int N, int group_size,
                            w4a16_dtype dtype, cudaStream_t stream);
@@ -153,10 +170,13 @@ w4a16_status nf4_dequant(const uint32_t* qweight, const float* absmax, const flo
  * ("GPTQ与bitsandbytes对比" GPTQ section: RTN is the plain baseline quantizer;
  * cloud.tencent.com/developer/article/2726413 §2.1-2.2).  Per group g and
  * column n, in fp64:
- *   mn = min(min_k w, 0), mx = max(max_k w, 0), s = RNE_fp16((mx - mn) / 15)
- *   (s = 1 if that is 0), z = clamp(rint(-mn / s), 0, 15),
- *   q = clamp(rint(w / s) + z, 0, 15)      (rint: half to even)
- * Outputs qweight [K/8, N], scales fp16 [K/128, N], qzeros [K/128, N/8].
+ *   asymmetric (qzeros given):
+ *     mn = min(min_k w, 0), mx = max(max_k w, 0), s = RNE_fp16((mx - mn) / 15)
+ *     (s = 1 if that is 0), z = clamp(rint(-mn / s), 0, 15),
+ *     q = clamp(rint(w / s) + z, 0, 15)      (rint: half to even)
+ *   symmetric (qzeros == NULL): s = RNE_fp16(max_k |w| / 7) (1 if 0),
+ *     q = clamp(rint(w / s), -8, 7) + 8
+ * Outputs qweight [K/8, N], scales fp16 [G, N], qzeros [G, N/8].
  */
 w4a16_status w4a16_quantize(const float* W, int K, int N, int group_size, uint32_t* qweight,
                             void* scales, uint32_t* qzeros, cudaStream_t stream);
@@ -186,7 +206,9 @@ w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const flo
  * scratch than that return W4A16_ERR_UNSUPPORTED (with the current split-K
  * plan every M <= 16 fits).  The function allocates and frees nothing.
  *  - The first call on each device looks up the array's address with that
- *    device current; make that first call before any stream capture.
+ *    device current and keeps it; make that first call before any stream
+ *    capture.  A cudaDeviceReset makes the kept address stale: do not call
+ *    this function on a device after resetting it in the same process.
  *  - Each call clears the scratch area that must start at zero, on `stream`.
  *  - All calls share the one array and it keeps the last call's contents:
  *    calls that may run at the same time on the GPU (different streams with
@@ -196,6 +218,36 @@ w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const flo
 w4a16_status w4a16_gemv_noalloc(const void* X, const uint32_t* qweight, const void* scales,
                                 const uint32_t* qzeros, const int32_t* g_idx, void* Y, int M, int N, int K,
                                 int group_size, w4a16_dtype dtype, int* dev_status, cudaStream_t stream);
+
+/*
+ * NF4 with double-quantized absmax: the same product as nf4_gemm with
+ * absmax = fl32(absmax_q * s2), s2 = absmax_s2[k/64, n/256] (see the format
+ * notes above; the 4-bit codes are those of the first level, computed with
+ * the original absmax).  absmax_q uint8 [K/64, N], absmax_s2 fp32
+ * [K/64, ceil(N/256)].  Other arguments as nf4_gemm.
+ */
+w4a16_status nf4dq_gemm(const void* X, const uint32_t* qweight, const uint8_t* absmax_q,
+                        const float* absmax_s2, const float* codebook16, void* Y, int M, int N, int K,
+                        int blocksize, w4a16_dtype dtype, void* workspace, size_t workspace_bytes,
+                        int* dev_status, cudaStream_t stream);
+
+/* W_out[K, N] (dtype) = W_hat for NF4 with double-quantized absmax;
+ * bit-exact with the definition above. */
+w4a16_status nf4dq_dequant(const uint32_t* qweight, const uint8_t* absmax_q, const float* absmax_s2,
+                           const float* codebook16, void* W_out, int K, int N, int blocksize,
+                           w4a16_dtype dtype, cudaStream_t stream);
+
+/*
+ * Second-level quantization of an NF4 absmax array [K/blocksize, N] (fp32):
+ * per row and block of 256 consecutive columns, s2 = fl32(max / 255) (the
+ * fp64 quotient rounded once to fp32; 1 if the block is all zero) and
+ * code = clamp(rint(absmax / s2), 0, 255) with the division in fp64.
+ * Outputs absmax_q uint8 [K/blocksize, N] and absmax_s2 fp32
+ * [K/blocksize, ceil(N/256)].  The pages do not describe bitsandbytes' own
+ * second level; this is the plain reading of "a scale of the scale".
+ */
+w4a16_status nf4_double_quantize(const float* absmax, int K, int N, int blocksize, uint8_t* absmax_q,
+                                 float* absmax_s2, cudaStream_t stream);
 
 /* Bytes of workspace w4a16_gemm / w4a16_gemv / nf4_gemm need for this
  * shape (0 when none is needed, and for shapes outside the size limits,

@@ -27,6 +27,7 @@
 #define PU(a) ((uint32_t*)(uintptr_t)(a))
 #define PF(a) ((float*)(uintptr_t)(a))
 #define PI(a) ((int32_t*)(uintptr_t)(a))
+#define PU8(a) ((uint8_t*)(uintptr_t)(a))
 
 static int defined_host_status(w4a16_status s) {
   return s == W4A16_OK || s == W4A16_ERR_INVALID_ARG || s == W4A16_ERR_UNSUPPORTED;
@@ -64,9 +65,13 @@ static int fuzz_sizes(void) {
                                                            dt, P(16), 1u << 20, NULL, NULL)));
             CHECK(defined_host_status(
                 nf4_gemm(NULL, PU(16), PF(16), PF(16), P(16), M, N, K, G, dt, NULL, 0, NULL, NULL)));
+            CHECK(defined_host_status(
+                nf4dq_gemm(NULL, PU(16), PU8(16), PF(16), PF(16), P(16), M, N, K, G, dt, NULL, 0, NULL, NULL)));
             if (a == 0) { /* the weight-only entry points take no M */
               CHECK(defined_host_status(w4a16_dequant(NULL, P(16), PU(16), NULL, P(16), K, N, G, dt, NULL)));
               CHECK(defined_host_status(nf4_dequant(NULL, PF(16), PF(16), P(16), K, N, G, dt, NULL)));
+              CHECK(defined_host_status(nf4dq_dequant(NULL, PU8(16), PF(16), PF(16), P(16), K, N, G, dt, NULL)));
+              CHECK(defined_host_status(nf4_double_quantize(NULL, K, N, G, PU8(16), PF(16), NULL)));
               if (d == 0) {
                 CHECK(defined_host_status(w4a16_quantize(NULL, K, N, G, PU(16), P(16), PU(16), NULL)));
                 CHECK(defined_host_status(nf4_quantize(NULL, K, N, G, PF(16), PU(16), PF(16), NULL)));
@@ -89,7 +94,8 @@ int main(void) {
       (fn_t)w4a16_workspace_bytes, (fn_t)w4a16_act_order_prepack,
       (fn_t)w4a16_gemm_prepacked, (fn_t)w4a16_prepacked_workspace_bytes,
       (fn_t)w4a16_selftest_wait_timeout, (fn_t)w4a16_status_string,
-      (fn_t)nf4_default_codebook,
+      (fn_t)nf4_default_codebook, (fn_t)nf4dq_gemm,
+      (fn_t)nf4dq_dequant,       (fn_t)nf4_double_quantize,
   };
   for (size_t i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i) CHECK(fns[i] != NULL);
 
@@ -117,7 +123,7 @@ int main(void) {
                    NULL) == W4A16_ERR_INVALID_ARG);
   CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, 60, 256, 128, W4A16_BF16, NULL, 0, NULL, NULL) ==
         W4A16_ERR_INVALID_ARG);
-  CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, 64, 256, 64, W4A16_BF16, NULL, 0, NULL, NULL) ==
+  CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), 4, 64, 384, 48, W4A16_BF16, NULL, 0, NULL, NULL) ==
         W4A16_ERR_UNSUPPORTED);
   CHECK(w4a16_gemm(NULL, PU(16), P(16), PU(16), NULL, P(16), 4, 64, 256, 128, W4A16_F16, NULL, 0, NULL, NULL) ==
         W4A16_ERR_INVALID_ARG);

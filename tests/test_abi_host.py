@@ -78,7 +78,8 @@ def test_validation_rejects_without_launch(lib):
     assert _gemm(lib, N=60) == INV  # N % 8
     assert _gemm(lib, K=260) == INV  # K % 8
     assert _gemm(lib, K=192) == INV  # K % group
-    assert _gemm(lib, K=256, g=64) == UNS  # group size other than 128
+    assert _gemm(lib, K=384, g=48) == UNS  # group size other than 32, 64, a multiple of 128 or K
+    assert _gemm(lib, K=256, g=16) == UNS
     assert _gemm(lib, K=0) == INV
     assert _gemm(lib, M=-1) == INV
     assert _gemm(lib, X=None) == INV  # null pointer
@@ -111,7 +112,7 @@ def test_validation_rejects_without_launch(lib):
     assert lib.w4a16_selftest_wait_timeout(16, 20 * 10**9, None) == INV
     # act-order prepack: no in-place reorder, group size, g_idx required
     assert lib.w4a16_act_order_prepack(16, 16, 256, 64, 128, 16, 32, None, None) == INV  # aliasing
-    assert lib.w4a16_act_order_prepack(16, 16, 256, 64, 64, 32, 48, None, None) == UNS
+    assert lib.w4a16_act_order_prepack(16, 16, 384, 64, 48, 32, 48, None, None) == UNS
     assert lib.w4a16_act_order_prepack(16, None, 256, 64, 128, 32, 48, None, None) == INV
     need = lib.w4a16_prepacked_workspace_bytes(4, 64, 256)
     assert need >= 4 * 256 * 2
