@@ -54,6 +54,8 @@ _SIGS = {
     "nf4dq_gemm": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
     "nf4dq_dequant": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "nf4_double_quantize": [_vp, _i, _i, _i, _vp, _vp, _vp],
+    "w4a16_repack_awq": [_vp, _vp, _i, _i, _i, _vp, _vp, _vp],
+    "w4a16_gemm_silu_mul": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -164,6 +166,23 @@ def gemv(X, qweight, scales, qzeros, g_idx=None, out=None, group_size=GROUP_SIZE
     return _int4_call("w4a16_gemv", X, qweight, scales, qzeros, g_idx, out, group_size, ws, dev_status)
 
 
+def gemm_silu_mul(X, qweight, scales, qzeros, out=None, group_size=GROUP_SIZE, ws=None, dev_status=None):
+    """A = SiLU(X . W_hat[:, :F]) * (X . W_hat[:, F:]) for a gate_up weight of
+    N = 2F columns (gate first), any M; returns A [M, F]."""
+    K = qweight.shape[0] * 8
+    N = qweight.shape[1]
+    _check_x(X, K)
+    M = X.shape[0]
+    A = _out(X, N // 2, out)
+    if ws is None:
+        ws = workspace(M, N, K, X.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _lib.w4a16_gemm_silu_mul(_ptr(X), _ptr(qweight), _ptr(scales), _ptr(qzeros), _ptr(A), M, N, K, group_size,
+                                  _DTYPES[X.dtype], _ptr(ws), nbytes, _ptr(dev_status), _stream(X.device))
+    _check(st, "w4a16_gemm_silu_mul")
+    return A
+
+
 def nf4_gemm(X, qweight, absmax, codebook=None, out=None, blocksize=NF4_BLOCK, ws=None, dev_status=None):
     """Y = X . W_hat (NF4), any M.  ``codebook`` None: the built-in table."""
     K = qweight.shape[0] * 8
@@ -194,6 +213,20 @@ def act_order_prepack(qweight, g_idx, group_size=GROUP_SIZE, dev_status=None):
                                       _ptr(dev_status), _stream(qweight.device))
     _check(st, "w4a16_act_order_prepack")
     return q_sorted, perm
+
+
+def repack_awq(qweight_awq, qzeros_awq, group_size=GROUP_SIZE):
+    """AWQ checkpoint (qweight int32 [K, N/8] and qzeros [K/g, N/8] packed
+    along N in AWQ's column order) -> (qweight [K/8, N], qzeros [K/g, N/8]) in
+    this library's layout; ``qzeros_awq`` None for symmetric weights."""
+    K, C = qweight_awq.shape
+    N = 8 * C
+    qweight = torch.empty((K // 8, N), dtype=torch.int32, device=qweight_awq.device)
+    qzeros = None if qzeros_awq is None else torch.empty_like(qzeros_awq)
+    st = _lib.w4a16_repack_awq(_ptr(qweight_awq), _ptr(qzeros_awq), K, N, group_size, _ptr(qweight), _ptr(qzeros),
+                               _stream(qweight_awq.device))
+    _check(st, "w4a16_repack_awq")
+    return qweight, qzeros
 
 
 def prepacked_workspace_bytes(M: int, N: int, K: int) -> int:

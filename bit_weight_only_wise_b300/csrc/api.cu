@@ -71,6 +71,10 @@ GemvArgs gemv_args(const void* X, const uint32_t* qw, void* Y, int M, int N, int
   a.K = K;
   a.KB = p.KB;
   a.blocks_n = p.blocks_n;
+  // the plain product: 256-column blocks (the fused SiLU entry overrides these)
+  a.cpb = kGemvCols;
+  a.hiofs = a.hi2 = kGemvCols / 2;
+  a.Nout = a.ldy = N;
   a.ctas = p.ctas;
   a.counters = static_cast<int*>(ws);
   a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kCountersBytes);
@@ -79,11 +83,19 @@ GemvArgs gemv_args(const void* X, const uint32_t* qw, void* Y, int M, int N, int
 
 w4a16_status int4_gemv_impl(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
                             const int32_t* g_idx, void* Y, int M, int N, int K, int group_size, w4a16_dtype dtype,
-                            void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
+                            void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream,
+                            bool silu = false) {
   const GemvPlan p = gemv_plan(M, N, K, g_idx ? kInt4Act : kInt4);
   w4a16_status st = check_workspace(p, workspace, workspace_bytes);
   if (st != W4A16_OK) return st;
   GemvArgs a = gemv_args(X, qweight, Y, M, N, K, p, workspace, dev_status);
+  if (silu) {  // gate columns [0, F), up columns [F, 2F): 128 output columns per block
+    a.silu = 1;
+    a.cpb = kGemvCols / 2;
+    a.hiofs = N / 2;
+    a.hi2 = 0;
+    a.Nout = a.ldy = N / 2;
+  }
   a.scales = static_cast<const uint16_t*>(scales);
   a.qz = qzeros;
   a.g_idx = g_idx;
@@ -203,6 +215,40 @@ w4a16_status nf4_gemm_impl(const void* X, const uint32_t* qweight, const float* 
 }  // namespace
 
 extern "C" {
+
+w4a16_status w4a16_gemm_silu_mul(const void* X, const uint32_t* qweight, const void* scales,
+                                 const uint32_t* qzeros, void* A, int M, int N, int K, int group_size,
+                                 w4a16_dtype dtype, void* workspace, size_t workspace_bytes, int* dev_status,
+                                 cudaStream_t stream) {
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_int4_shape(M, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (N % 16) return W4A16_ERR_INVALID_ARG;  // F = N / 2 a multiple of 8
+  if (M == 0 || N == 0) return W4A16_OK;
+  st = check_int4_ptrs(X, qweight, scales, qzeros, nullptr, A);
+  if (st != W4A16_OK) return st;
+  if (M <= W4A16_GEMV_MAX_M)
+    return int4_gemv_impl(X, qweight, scales, qzeros, nullptr, A, M, N, K, group_size, dtype, workspace,
+                          workspace_bytes, dev_status, stream, true);
+  st = check_gemm_workspace(gemm_split_plan(M, N, K, false), workspace, workspace_bytes);
+  if (st != W4A16_OK) return st;
+  GemmArgs a{};
+  a.X = X;
+  a.qw = qweight;
+  a.scales = static_cast<const uint16_t*>(scales);
+  a.qz = qzeros;
+  a.Y = static_cast<uint16_t*>(A);
+  a.dev_status = dev_status;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.gsize = group_size;
+  a.NG = K / group_size;
+  a.silu = 1;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return from_cuda(launch_gemm_tc(a, dtype == W4A16_BF16, false, stream));
+}
 
 w4a16_status nf4_gemm(const void* X, const uint32_t* qweight, const float* absmax, const float* codebook16,
                       void* Y, int M, int N, int K, int blocksize, w4a16_dtype dtype, void* workspace,
@@ -341,6 +387,18 @@ w4a16_status w4a16_gemm_prepacked(const void* X, const uint32_t* qweight_sorted,
   if (e != cudaSuccess) return W4A16_ERR_CUDA;
   return w4a16_gemm(Xp, qweight_sorted, scales, qzeros, nullptr, Y, M, N, K, group_size, dtype,
                     plain ? workspace : nullptr, plain, dev_status, stream);
+}
+
+w4a16_status w4a16_repack_awq(const uint32_t* qweight_awq, const uint32_t* qzeros_awq, int K, int N, int group_size,
+                              uint32_t* qweight, uint32_t* qzeros, cudaStream_t stream) {
+  w4a16_status st = check_int4_shape(0, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (N == 0) return W4A16_OK;
+  if (!ok_ptr(qweight_awq) || !ok_ptr(qweight)) return W4A16_ERR_INVALID_ARG;
+  if (!qzeros_awq != !qzeros) return W4A16_ERR_INVALID_ARG;  // both or neither (symmetric)
+  if (qzeros_awq && (!aligned16(qzeros_awq) || !aligned16(qzeros))) return W4A16_ERR_INVALID_ARG;
+  if (qweight == qweight_awq || (qzeros && qzeros == qzeros_awq)) return W4A16_ERR_INVALID_ARG;  // not in place
+  return from_cuda(launch_awq_repack(qweight_awq, qzeros_awq, K, N, K / group_size, qweight, qzeros, stream));
 }
 
 const char* w4a16_status_string(w4a16_status status) {

@@ -112,10 +112,19 @@ struct GemmParams {
   uint16_t* Y;
   int* dev_status;
   int M, N, K;
+  // Columns.  A CTA's 128 TMEM lanes are two halves of 64: lane l reads weight
+  // column tile * cpt + (l / 64) hiofs + l % 64 and makes output column
+  // tile * cpt + (l / 64) hi2 + l % 64.  Plain product: cpt = 128, hiofs =
+  // hi2 = 64.  Fused SiLU(gate) * up (silu): the gate half and the matching
+  // up half, cpt = 64, hiofs = F = N / 2, hi2 = 0, and the epilogue pairs them.
+  int silu, cpt, hiofs, hi2, Nout, ldy;
   int BT;
   int token_fast;
   uint32_t idesc;
 };
+
+// SiLU(g) * u in fp32, the gate_up epilogue
+__device__ __forceinline__ float silu_mul_f32(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
 
 template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -136,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // token tiles vary fastest: the CTAs that share a weight tile run together
   // and the weights come from DRAM about once.  Otherwise column tiles vary
   // fastest and the (then L2-resident) weights are shared across a wave.
-  const int n0 = (p.token_fast ? blockIdx.y : blockIdx.x) * kBN;
+  const int w0 = (p.token_fast ? blockIdx.y : blockIdx.x) * p.cpt;  // first weight (and output) column
   const int m0 = (p.token_fast ? blockIdx.x : blockIdx.y) * p.BT;
   // Split-K: CTA z of a tile takes K blocks [kb0, kb0 + nkb) (group aligned)
   const int kb_total = (p.K + kBK - 1) / kBK;
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (FMT == kFmtInt4Act) {
     const int G = p.NG;
     for (int i = threadIdx.x; i < G * kBN; i += kThreads) {
-      const int g = i / kBN, c = i % kBN, n = n0 + c;
+      const int g = i / kBN, c = i % kBN, n = w0 + (c >> 6) * p.hiofs + (c & 63);
       uint32_t v = 0;
       if (n < p.N) {
         const uint32_t sb = p.scales[(size_t)g * p.N + n];
@@ -192,7 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->empty[s], ((it / kStages) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) break;
         mbar_arrive_expect_tx(&bars->full[s], tx);
         tma_load_2d(sx + s * kXStageBytes, &tmX, &bars->full[s], (kb0 + it) * kBK, m0);
-        tma_load_2d(sw + s * (kWStageBytes / 4), &tmW, &bars->full[s], n0, (kb0 + it) * (kBK / 8));
+        // the two 64-column halves of the tile, one box each
+        tma_load_2d(sw + s * (kWStageBytes / 4), &tmW, &bars->full[s], w0, (kb0 + it) * (kBK / 8));
+        tma_load_2d(sw + s * (kWStageBytes / 4) + kWStageBytes / 8, &tmW, &bars->full[s], w0 + p.hiofs,
+                    (kb0 + it) * (kBK / 8));
         issued = it + 1;
       }
       if (*abort) {
@@ -228,8 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (dw % kGroupWarps) >> 2;     // which kWords word-rows of a stage
     const int ep = dw >> 2;                    // epilogue: which quarter of the tokens
     const int nl = quarter * 32 + lane;
-    const int n = n0 + nl;
-    const bool ok = n < p.N;
+    const int n = w0 + (nl >> 6) * p.hiofs + (nl & 63);     // weight column
+    const int ocol = w0 + (nl >> 6) * p.hi2 + (nl & 63);    // output column
+    const bool ok = ocol < p.Nout;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
     // the current K block's constants, with the raw values of this group's
@@ -294,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t wv[kWords];
       const uint32_t* wst = sw + s * (kWStageBytes / 4);
 #pragma unroll
-      for (int i = 0; i < kWords; ++i) wv[i] = wst[(kWords * h + i) * kBN + nl];
+      for (int i = 0; i < kWords; ++i) wv[i] = wst[(nl >> 6) * (kBN / 2) * (kBK / 8) + (kWords * h + i) * (kBN / 2) + (nl & 63)];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->empty[s]);
       uint32_t regs[4 * kWords];
@@ -351,11 +364,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA in flight before TMEM is freed.
     const bool done = mbar_drain(&bars->d_full, 0, kDrainLimitNs);
     tc_fence_after();
+    // Fused SiLU: every lane's fp32 results pass through shared memory (the
+    // X ring, idle once the MMAs are done: BT x 128 floats), then the gate
+    // lanes pair them with the up lanes'.
+    float* xb = reinterpret_cast<float*>(sx);
+    const int part = p.BT / kParts;  // tokens per warp, a multiple of 8
+    auto emit = [&](int c, const float (&v)[8]) {  // tokens c .. c+7 of this lane
+      if (p.silu) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xb[(size_t)(c + j) * kBN + nl] = v[j];
+      } else if (ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int m = m0 + c + j;
+          if (m < p.M) p.Y[(size_t)m * p.ldy + ocol] = (uint16_t)(pack2_rn(v[j], 0.f, BF16) & 0xFFFFu);
+        }
+      }
+    };
+    bool emitted = false;
     if (done && !*abort && p.splits > 1) {
       // Split-K: this CTA's fp32 tile goes to the workspace; the CTA that
       // completes the tile's ticket sums the splits in split order
       // (deterministic) and writes Y.
-      const int part = p.BT / kParts;
       const int tile = (int)(blockIdx.x + gridDim.x * blockIdx.y);
       const size_t tile_floats = (size_t)p.BT * kBN;
       float* mine = p.partial + ((size_t)tile * p.splits + blockIdx.z) * tile_floats;
@@ -372,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bars->last = ticket_inc_acquire(p.counters + tile, (uint32_t)(p.splits - 1)) == (uint32_t)(p.splits - 1);
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
-      if (bars->last && ok) {
+      if (bars->last && (ok || p.silu)) {
         const float* base = p.partial + (size_t)tile * p.splits * tile_floats;
         for (int c = ep * part; c < (ep + 1) * part; c += 8) {
           float acc[8];
@@ -394,27 +424,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < 8; ++j)
                 if (z0 + zz < p.splits) acc[j] += v[zz][j];
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int m = m0 + c + j;
-            if (m < p.M) p.Y[(size_t)m * p.N + n] = (uint16_t)(pack2_rn(acc[j], 0.f, BF16) & 0xFFFFu);
-          }
+          emit(c, acc);
         }
       }
+      emitted = bars->last != 0;
     } else if (done && !*abort) {
-      const int part = p.BT / kParts;  // tokens per warp, a multiple of 8
       for (int c = ep * part; c < (ep + 1) * part; c += 8) {
         uint32_t v[8];
         tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
         tmem_wait_ld();
-        if (ok) {
+        float f[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int m = m0 + c + j;
-            if (m < p.M) {
-              const uint32_t y = pack2_rn(__uint_as_float(v[j]), 0.f, BF16);
-              p.Y[(size_t)m * p.N + n] = (uint16_t)(y & 0xFFFFu);
-            }
+        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+        emit(c, f);
+      }
+      emitted = true;
+    }
+    if (p.silu && emitted) {  // a CTA-uniform condition: every dequant warp gets here or none
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+      if (nl < kBN / 2 && ok) {
+        for (int t = ep * part; t < (ep + 1) * part; ++t) {
+          const int m = m0 + t;
+          if (m < p.M) {
+            const float act = silu_mul_f32(xb[(size_t)t * kBN + nl], xb[(size_t)t * kBN + kBN / 2 + nl]);
+            p.Y[(size_t)m * p.ldy + ocol] = (uint16_t)(pack2_rn(act, 0.f, BF16) & 0xFFFFu);
           }
         }
       }
@@ -490,7 +523,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.qw, (uint64_t)a.N, (uint64_t)(a.K / 8), (uint64_t)a.N * 4,
-                 kBN, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+                 kBN / 2, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   GemmParams p{};
   p.g_idx = a.g_idx;
@@ -526,7 +559,12 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
     p.counters = static_cast<int*>(a.workspace);
     p.partial = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + kCountersBytes);
   }
-  const unsigned col_tiles = (a.N + kBN - 1) / kBN, tok_tiles = (a.M + BT - 1) / BT;
+  p.silu = a.silu;
+  p.cpt = a.silu ? kBN / 2 : kBN;
+  p.hiofs = a.silu ? a.N / 2 : kBN / 2;
+  p.hi2 = a.silu ? 0 : kBN / 2;
+  p.Nout = p.ldy = a.silu ? a.N / 2 : a.N;
+  const unsigned col_tiles = (p.Nout + p.cpt - 1) / p.cpt, tok_tiles = (a.M + BT - 1) / BT;
   p.token_fast = (size_t)a.K * a.N / 2 > (size_t)64 << 20;
   dim3 grid = p.token_fast ? dim3(tok_tiles, col_tiles, sp.splits) : dim3(col_tiles, tok_tiles, sp.splits);
   if (nf4) return bf16 ? launch_tc<kFmtNF4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtNF4, false>(tmX, tmW, p, grid, st);

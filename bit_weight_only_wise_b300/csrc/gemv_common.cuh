@@ -3,11 +3,15 @@
 // tensor-core step, and the write-out of a finished 256-column block, either
 // directly or through the deterministic split-K reduction.
 //
-// Units: 256 output columns x one 128-row K group, numbered column-block-major
-// (u = b * G + g).  CTA i of P owns units [U*i/P, U*(i+1)/P).  Within a CTA,
+// Units: 256 weight columns x one 128-row K block, numbered column-block-major
+// (u = b * KB + kb).  CTA i of P owns units [U*i/P, U*(i+1)/P).  Within a CTA,
 // 8 warps own a 32-column slice each; lane (g, c) = (lane / 4, lane % 4)
 // accumulates columns 4g .. 4g+3 of the slice for tokens 2c, 2c+1 (+8t) in
 // the m16n8k16 accumulator layout (column = MMA row, token = MMA column).
+// Slice w of block b is output column b * cpb + 32 (w % 4) + (w / 4) hi2 on
+// (see GemvArgs): the plain product's 256 columns, or with the fused SiLU
+// epilogue the gate (w < 4) and up (w >= 4) halves of 128 output columns,
+// which the write-out pairs: act = SiLU(gate) * up.
 #pragma once
 
 #include <cstdint>
@@ -27,6 +31,14 @@ struct Range {
   // the CTA whose range holds unit u: the largest i with start(i) <= u
   __device__ __forceinline__ int owner(long long u) const { return (int)(((u + 1) * P - 1) / U); }
 };
+
+// SiLU(g) * u in fp32, the gate_up epilogue
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
+
+// first output column of warp w's slice of block b
+__device__ __forceinline__ int slice_col(const GemvArgs& a, int b, int warp) {
+  return b * a.cpb + 32 * (warp & 3) + (warp >> 2) * a.hi2;
+}
 
 template <bool BF16>
 __device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
@@ -64,31 +76,10 @@ __device__ __forceinline__ void x_pairs(const uint4& xv, uint32_t bf[4]) {
 // first block, 1 for its last) and the function returns true: the block's
 // ticket is taken later, by finish_blocks, once the CTA has nothing else to
 // do, so that no warp waits on a memory round trip in the middle of its work.
-template <int NT, bool BF16>
-__device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, int cta, int first_block, int warp,
-                                            int lane, int b, const float (&acc)[NT][2][4]) {
+// this warp's fp32 fragment of a block into a slice slot (the split-K layout)
+template <int NT>
+__device__ __forceinline__ void store_slot(const GemvArgs& a, float* slot, int lane, const float (&acc)[NT][2][4]) {
   const int gl = lane >> 2, c = lane & 3;
-  const int col0 = b * kGemvCols + warp * 32 + 4 * gl;
-  const int i_first = R.owner((long long)b * a.KB);
-  const int i_last = R.owner((long long)(b + 1) * a.KB - 1);
-  if (i_first == i_last) {
-    if (col0 >= a.N) return false;
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int tok = 8 * t + 2 * c;
-        const int col = col0 + 2 * r;
-        if (tok < a.M)
-          *reinterpret_cast<uint32_t*>(a.Y + (size_t)tok * a.N + col) = pack2_rn(acc[t][r][0], acc[t][r][2], BF16);
-        if (tok + 1 < a.M)
-          *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * a.N + col) =
-              pack2_rn(acc[t][r][1], acc[t][r][3], BF16);
-      }
-    return false;
-  }
-  const int seg = (b == first_block) ? 0 : 1;
-  float* slot = a.partial + ((size_t)(cta * 2 + seg) * kSliceWarps + warp) * a.M * 32;
 #pragma unroll
   for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -99,6 +90,67 @@ __device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, i
       if (tok + 1 < a.M)
         *reinterpret_cast<float2*>(slot + (tok + 1) * 32 + cl) = make_float2(acc[t][r][1], acc[t][r][3]);
     }
+}
+
+// Slot of CTA cta's segment seg (0: its first block, 1: its last), slice w.
+// With the fused SiLU epilogue the grid holds at most 2 CTAs per SM; the
+// workspace is sized for kGemvMaxCTAsPerSM (3), so the slots of CTA indices
+// kNumSMs * 2 .. kNumSMs * 3 - 1 are unused by the split-K reduction, and
+// (CTA kNumSMs * 2 + i / 2, segment i % 2) carries CTA i's fully owned
+// blocks' gate and up halves between its warps.
+static_assert(kGemvMaxCTAsPerSM >= 3, "the SiLU exchange slots lie past two CTAs per SM");
+__device__ __forceinline__ float* slice_slot(const GemvArgs& a, int cta, int seg, int warp) {
+  return a.partial + ((size_t)(cta * 2 + seg) * kSliceWarps + warp) * a.M * 32;
+}
+
+// Warp `warp`'s slice of column block b is finished.  When CTA `cta` owns
+// the whole block the slice is rounded and written to Y here.  Otherwise its
+// fp32 partial goes to the CTA's slot for the block (slot 0 for the CTA's
+// first block, 1 for its last) and the function returns true: the block's
+// ticket is taken later, by finish_blocks, once the CTA has nothing else to
+// do, so that no warp waits on a memory round trip in the middle of its work.
+// Fused SiLU, whole block: both halves pass through the CTA's exchange slot,
+// a barrier of the consumer warps (named barrier 1, all kSliceWarps warps)
+// orders the writes before the gate warps read.
+template <int NT, bool BF16>
+__device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, int cta, int first_block, int warp,
+                                            int lane, int b, const float (&acc)[NT][2][4]) {
+  const int gl = lane >> 2, c = lane & 3;
+  const int col0 = slice_col(a, b, warp) + 4 * gl;
+  const int i_first = R.owner((long long)b * a.KB);
+  const int i_last = R.owner((long long)(b + 1) * a.KB - 1);
+  if (i_first == i_last && a.silu) {
+    float* xs = slice_slot(a, kNumSMs * 2 + cta / 2, cta % 2, 0);
+    store_slot<NT>(a, xs + (size_t)warp * a.M * 32, lane, acc);
+    asm volatile("bar.sync 1, %0;" ::"r"(kSliceWarps * 32) : "memory");
+    if (warp < kSliceWarps / 2) {
+      const int col = slice_col(a, b, warp) + lane;
+      const float* gp = xs + (size_t)warp * a.M * 32 + lane;
+      const float* up = xs + (size_t)(warp + kSliceWarps / 2) * a.M * 32 + lane;
+      if (col < a.Nout)
+        for (int t = 0; t < a.M; ++t)
+          a.Y[(size_t)t * a.ldy + col] = (uint16_t)(pack2_rn(silu_mul(gp[t * 32], up[t * 32]), 0.f, BF16) & 0xFFFFu);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kSliceWarps * 32) : "memory");  // the slot is free again
+    return false;
+  }
+  if (i_first == i_last) {
+    if (col0 >= a.Nout) return false;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int tok = 8 * t + 2 * c;
+        const int col = col0 + 2 * r;
+        if (tok < a.M)
+          *reinterpret_cast<uint32_t*>(a.Y + (size_t)tok * a.ldy + col) = pack2_rn(acc[t][r][0], acc[t][r][2], BF16);
+        if (tok + 1 < a.M)
+          *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * a.ldy + col) =
+              pack2_rn(acc[t][r][1], acc[t][r][3], BF16);
+      }
+    return false;
+  }
+  store_slot<NT>(a, slice_slot(a, cta, b == first_block ? 0 : 1, warp), lane, acc);
   return true;
 }
 
@@ -109,8 +161,8 @@ __device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, i
 // can.  Several contributors' loads are in flight at once.
 template <int NT, bool BF16>
 __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, int warp, int lane, int b) {
-  const int col = b * kGemvCols + warp * 32 + lane;
-  if (col >= a.N) return;
+  const int col = slice_col(a, b, warp) + lane;
+  if (col >= a.Nout) return;
   const int i_first = R.owner((long long)b * a.KB);
   const int i_last = R.owner((long long)(b + 1) * a.KB - 1);
   const int sg_first = R.start(i_first) == (long long)b * a.KB ? 0 : 1;
@@ -118,6 +170,17 @@ __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, 
   auto slot = [&](int i) -> const float* {
     return a.partial + ((size_t)(i * 2 + (i == i_first ? sg_first : 0)) * kSliceWarps + warp) * stride + lane;
   };
+  if (a.silu) {  // slices warp (gate) and warp + 4 (up), both summed in contributor order
+    for (int t = 0; t < a.M; ++t) {
+      float g = 0.f, u = 0.f;
+      for (int i = i_first; i <= i_last; ++i) {
+        g += __ldcg(slot(i) + t * 32);
+        u += __ldcg(slot(i) + (size_t)(kSliceWarps / 2) * stride + t * 32);
+      }
+      a.Y[(size_t)t * a.ldy + col] = (uint16_t)(pack2_rn(silu_mul(g, u), 0.f, BF16) & 0xFFFFu);
+    }
+    return;
+  }
   if (a.M == 1) {  // single token: sixteen contributors per round trip
     float sum = 0.f;
     for (int i0 = i_first; i0 <= i_last; i0 += 16) {
@@ -150,7 +213,7 @@ __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, 
   }
 #pragma unroll
   for (int t = 0; t < 8 * NT; ++t)
-    if (t < a.M) a.Y[(size_t)t * a.N + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
+    if (t < a.M) a.Y[(size_t)t * a.ldy + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
 }
 
 // reduce_block for two blocks at M = 1 with every contributor's load of both
@@ -165,7 +228,7 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
     first[h] = R.owner((long long)bs[h] * a.KB);
     last[h] = R.owner((long long)(bs[h] + 1) * a.KB - 1);
     sgf[h] = R.start(first[h]) == (long long)bs[h] * a.KB ? 0 : 1;
-    col[h] = bs[h] * kGemvCols + warp * 32 + lane;
+    col[h] = slice_col(a, bs[h], warp) + lane;
   }
   float sum[2] = {0.f, 0.f};
   const int n = max(last[0] - first[0], last[1] - first[1]) + 1;
@@ -178,7 +241,7 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
         const int i = first[h] + j0 + j;
         const float* pp =
             a.partial + ((size_t)(i * 2 + (i == first[h] ? sgf[h] : 0)) * kSliceWarps + warp) * 32 + lane;
-        v[h][j] = (i <= last[h] && col[h] < a.N) ? __ldcg(pp) : 0.f;
+        v[h][j] = (i <= last[h] && col[h] < a.Nout) ? __ldcg(pp) : 0.f;
       }
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -187,7 +250,7 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h)
-    if (col[h] < a.N) a.Y[col[h]] = (uint16_t)(pack2_rn(sum[h], 0.f, BF16) & 0xFFFFu);
+    if (col[h] < a.Nout) a.Y[col[h]] = (uint16_t)(pack2_rn(sum[h], 0.f, BF16) & 0xFFFFu);
 }
 
 // The CTA is done: publish this warp's partials of split blocks p0 and p1
@@ -200,21 +263,32 @@ __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R,
   // fence, whose release covers them before the tickets move; the acquire
   // increments order the summing loads after the other contributors' stores
   __syncwarp();
+  // Fused SiLU: the gate slice w and the up slice w + 4 of every contributor
+  // count on one ticket (slice w % 4), so the warp that completes it sums
+  // both halves: a wrap of 2 contributors - 1.
   int last0 = 0, last1 = 0;
   if (lane == 0) {
     __threadfence();
+    const int tw = a.silu ? (warp & (kSliceWarps / 2 - 1)) : warp;
     if (p0 >= 0) {
-      const uint32_t w = (uint32_t)(R.owner((long long)(p0 + 1) * a.KB - 1) - R.owner((long long)p0 * a.KB));
-      last0 = sm100::ticket_inc_acquire(a.counters + p0 * kSliceWarps + warp, w) == w;
+      uint32_t w = (uint32_t)(R.owner((long long)(p0 + 1) * a.KB - 1) - R.owner((long long)p0 * a.KB));
+      if (a.silu) w = 2 * w + 1;
+      last0 = sm100::ticket_inc_acquire(a.counters + p0 * kSliceWarps + tw, w) == w;
     }
     if (p1 >= 0) {
-      const uint32_t w = (uint32_t)(R.owner((long long)(p1 + 1) * a.KB - 1) - R.owner((long long)p1 * a.KB));
-      last1 = sm100::ticket_inc_acquire(a.counters + p1 * kSliceWarps + warp, w) == w;
+      uint32_t w = (uint32_t)(R.owner((long long)(p1 + 1) * a.KB - 1) - R.owner((long long)p1 * a.KB));
+      if (a.silu) w = 2 * w + 1;
+      last1 = sm100::ticket_inc_acquire(a.counters + p1 * kSliceWarps + tw, w) == w;
     }
   }
   __syncwarp();
   last0 = __shfl_sync(0xFFFFFFFFu, last0, 0);
   last1 = __shfl_sync(0xFFFFFFFFu, last1, 0);
+  if (a.silu) {  // the completing warp may be the gate or the up one: sum from the gate slice
+    if (last0) reduce_block<NT, BF16>(a, R, warp & (kSliceWarps / 2 - 1), lane, p0);
+    if (last1) reduce_block<NT, BF16>(a, R, warp & (kSliceWarps / 2 - 1), lane, p1);
+    return;
+  }
   if (last0 && last1 && a.M == 1) {  // both blocks: one round trip for the two
     reduce_two_blocks_m1<BF16>(a, R, warp, lane, p0, p1);
     return;

@@ -218,6 +218,14 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   const int nw = a.N >> 3;  // zero words per row
   const int nb64 = a.K / 64;
   const int nc2 = (a.N + kGemvCols - 1) / kGemvCols;
+  // this lane's constant column offsets within a block (see GemvArgs: the
+  // unit's second half starts a.hiofs weight columns and a.hi2 output
+  // columns after its first): its weight box (lanes < 8), its 8 scales, their
+  // output column, and their zero word
+  const int wcol_l = 32 * (lane & 3) + (lane >> 2) * a.hiofs;
+  const int scol_l = 8 * (lane & 15) + (lane >> 4) * a.hiofs;
+  const int ocol_l = 8 * (lane & 15) + (lane >> 4) * a.hi2;
+  const int zw_l = (lane >> 4) * (a.hiofs >> 3) + (lane & 15);
   // the unit's metadata into stage s, by cp.async (NF4's absmax by TMA)
   auto issue_meta = [&](int s, const UnitWalk<GPU>& u) {
     const uint32_t side = side0 + s * L::SIDE;
@@ -227,14 +235,14 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
       for (int j = 0; j < L::NGRP; ++j) {
         const int gi = u.group(j);
         const bool gv = GPU <= 1 || gi < a.NG;  // only 32/64-row groups can run past K
-        const int col = b * kGemvCols + 8 * lane;
-        const bool sv = gv && col < a.N;
+        const int col = b * a.cpb + scol_l;
+        const bool sv = gv && b * a.cpb + ocol_l < a.Nout;
         cp_async_16(side + L::RAW + j * (kGemvCols * 2) + 16 * lane, sv ? a.scales + (size_t)gi * a.N + col : a.scales,
                     sv);
         // symmetric weights: a.nwz = 0, so the zero words are zero-filled
         // (the helper turns them into 8s)
-        const int zc = b * 32 + lane;
-        const bool zv = gv && zc < a.nwz;
+        const int zc = b * (a.cpb >> 3) + zw_l;
+        const bool zv = sv && zc < a.nwz;
         cp_async_4(side + L::RAW + L::NGRP * (kGemvCols * 2) + j * 128 + 4 * lane,
                    zv ? a.qz + (size_t)gi * nw + zc : a.qw, zv);
       }
@@ -268,7 +276,7 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
     if (lane == 0) mbar_arrive_expect_tx(&full[s], L::TX);
     __syncwarp();
     if (lane < kCW)
-      tma_load_2d(smem + s * kWBytes + lane * kWBox, tmW, &full[s], u.b * kGemvCols + lane * 32, u.kb * 16);
+      tma_load_2d(smem + s * kWBytes + lane * kWBox, tmW, &full[s], u.b * a.cpb + wcol_l, u.kb * 16);
     if (lane == 0) tma_load_2d(smem + S * kWBytes + s * L::SIDE + L::X, tmX, &full[s], u.kb * 128, 0);
     issue_meta(s, u);
   };
@@ -285,14 +293,14 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   {
     UnitWalk<GPU> u(a, b0, k0);
     for (int k = 0; k < n_first; ++k) {
-      if (lane < kCW) tma_prefetch_l2_2d(tmW, u.b * kGemvCols + lane * 32, u.kb * 16);
+      if (lane < kCW) tma_prefetch_l2_2d(tmW, u.b * a.cpb + wcol_l, u.kb * 16);
       if constexpr (FMT == kInt4) {
-        const int col = u.b * kGemvCols + 8 * lane;
+        const int col = u.b * a.cpb + scol_l;
 #pragma unroll
         for (int j = 0; j < L::NGRP; ++j) {
           const int gi = u.group(j);
-          if (gi < a.NG && col < a.N) prefetch_l2(a.scales + (size_t)gi * a.N + col);
-          if (gi < a.NG && a.nwz && lane == 0) prefetch_l2(a.qz + (size_t)gi * nw + u.b * 32);
+          if (gi < a.NG && u.b * a.cpb + ocol_l < a.Nout) prefetch_l2(a.scales + (size_t)gi * a.N + col);
+          if (gi < a.NG && a.nwz && (lane & 15) == 0) prefetch_l2(a.qz + (size_t)gi * nw + u.b * (a.cpb >> 3) + zw_l);
         }
       } else if constexpr (FMT == kNF4) {
         if (lane == kCW) tma_prefetch_l2_2d(tmA, u.b * kGemvCols, u.kb * 2);

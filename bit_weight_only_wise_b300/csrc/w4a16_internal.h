@@ -69,6 +69,14 @@ struct GemvArgs {
   int gsize;       // rows per group (INT4)
   int kbpg;        // 128-row units per group (set by the launcher)
   int nwz;         // zero words per row to copy: N / 8, or 0 for symmetric weights (launcher)
+  // Output columns.  Plain product: a column block is 256 output columns, the
+  // unit's second half starting 128 columns on (cpb = 256, hiofs = hi2 = 128,
+  // Nout = ldy = N).  Fused SiLU(gate) * up (silu = 1): the weight holds gate
+  // columns [0, F) then up columns [F, 2F); a block is 128 output columns,
+  // its unit the 128 gate columns then the 128 matching up columns (cpb =
+  // 128, hiofs = F, hi2 = 0, Nout = ldy = F = N / 2).
+  int silu;
+  int cpb, hiofs, hi2, Nout, ldy;
   uint32_t zxor;   // 0, or 0x88888888 for symmetric weights: zero points of 8 (launcher)
   int blocks_n;    // 256-column blocks
   int ctas;
@@ -100,6 +108,7 @@ struct GemmArgs {
   const int32_t* g_idx;    // INT4 act-order map or nullptr
   int gsize;               // INT4 rows per group
   int NG;                  // INT4 groups along K
+  int silu;                // fused SiLU(gate) * up: Y [M, N/2] from gate [0, N/2) and up [N/2, N)
   const float* absmax;     // NF4
   const uint8_t* absmax_q; // NF4 double quantization: 8-bit codes [K/64, N], or nullptr
   const float* absmax_s2;  // NF4 double quantization: fp32 [K/64, ceil(N/256)]
@@ -144,6 +153,10 @@ cudaError_t launch_act_order_prepack(const uint32_t* qw, const int32_t* g_idx, i
                                      uint32_t* qw_sorted, int32_t* perm, int* dev_status, cudaStream_t st);
 cudaError_t launch_gather_columns(const uint16_t* X, const int32_t* perm, int M, int K, uint16_t* out,
                                   cudaStream_t st);
+
+// ------------------------------------------------------------ AWQ layout
+cudaError_t launch_awq_repack(const uint32_t* qweight_awq, const uint32_t* qzeros_awq, int K, int N, int G,
+                              uint32_t* qweight, uint32_t* qzeros, cudaStream_t st);
 
 // ------------------------------------------------------- standalone kernels
 cudaError_t launch_dequant_int4(const uint32_t* qw, const uint16_t* scales, const uint32_t* qz,

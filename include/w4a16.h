@@ -145,6 +145,23 @@ w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scal
                         void* workspace, size_t workspace_bytes, int* dev_status,
                         cudaStream_t stream);
 
+/*
+ * Fused decoder-MLP activation: A[M, F] = SiLU(X . W_hat[:, :F]) * (X . W_hat[:, F:])
+ * for a gate_up weight of N = 2F columns (gate in columns [0, F), up in
+ * [F, 2F)), SiLU(t) = t / (1 + e^-t), both products and the activation in
+ * fp32 and one rounding of A to dtype.  The 2F-wide product never goes to
+ * memory: per-token latency follows the bytes moved per forward
+ * ("LLM量化技术深度对比" key-data items 1 and 3), and the activation is the
+ * gate_up product's epilogue.  The pages do not spell the layer out; the
+ * gate-then-up column order is this library's reading.
+ *   A: [M, N/2] in dtype; N a multiple of 16.  No act-order map (prepack such
+ *   checkpoints).  Other arguments, workspace and limits as w4a16_gemm.
+ */
+w4a16_status w4a16_gemm_silu_mul(const void* X, const uint32_t* qweight, const void* scales,
+                                 const uint32_t* qzeros, void* A, int M, int N, int K, int group_size,
+                                 w4a16_dtype dtype, void* workspace, size_t workspace_bytes, int* dev_status,
+                                 cudaStream_t stream);
+
 /* Y = X . W_hat for the NF4 format, any M >= 0.  blocksize: 64.
  * codebook16: a device table of 16 fp32 values, or NULL for the library's
  * built-in table (nf4_default_codebook).  Other arguments as w4a16_gemm. */
@@ -295,6 +312,25 @@ w4a16_status w4a16_gemm_prepacked(const void* X, const uint32_t* qweight_sorted,
 /* Bytes of workspace w4a16_gemm_prepacked needs (0 for shapes outside the
  * size limits).  Pure host function. */
 size_t w4a16_prepacked_workspace_bytes(int M, int N, int K);
+
+/*
+ * Repack an AWQ checkpoint ("模型量化实践" §3.1: zero_point=True,
+ * q_group_size, w_bit=4, version="GEMM"; served by a faster kernel's layout
+ * in "LLM量化技术深度对比" §5) into this library's layout, once at load.
+ * The pages do not print AWQ's packing; the layout read here is AWQ's
+ * published GEMM layout (equality with files written by AWQ's own tools is
+ * not verified here):
+ *   qweight_awq int32 [K, N/8]: word [k, c] = row k, columns 8c .. 8c+7, with
+ *                               column 8c + ORDER[j] in bits 4j .. 4j+3,
+ *                               ORDER = (0, 2, 4, 6, 1, 3, 5, 7)
+ *   qzeros_awq  int32 [G, N/8]: zero points packed the same way (NULL for
+ *                               symmetric weights, with qzeros NULL too)
+ * Outputs qweight [K/8, N] and qzeros [G, N/8] in this library's layout
+ * (caller-owned device buffers, not aliasing the inputs); the fp16 scales
+ * [G, N] are already in this library's layout.  G = K / group_size.
+ */
+w4a16_status w4a16_repack_awq(const uint32_t* qweight_awq, const uint32_t* qzeros_awq, int K, int N,
+                              int group_size, uint32_t* qweight, uint32_t* qzeros, cudaStream_t stream);
 
 /*
  * Self-test of the bounded device-side wait that every pipeline wait in this

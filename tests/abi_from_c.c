@@ -65,6 +65,8 @@ static int fuzz_sizes(void) {
                                                            dt, P(16), 1u << 20, NULL, NULL)));
             CHECK(defined_host_status(
                 nf4_gemm(NULL, PU(16), PF(16), PF(16), P(16), M, N, K, G, dt, NULL, 0, NULL, NULL)));
+            CHECK(defined_host_status(w4a16_gemm_silu_mul(NULL, PU(16), P(16), PU(16), P(16), M, N, K, G, dt, NULL, 0,
+                                                          NULL, NULL)));
             CHECK(defined_host_status(
                 nf4dq_gemm(NULL, PU(16), PU8(16), PF(16), PF(16), P(16), M, N, K, G, dt, NULL, 0, NULL, NULL)));
             if (a == 0) { /* the weight-only entry points take no M */
@@ -72,6 +74,7 @@ static int fuzz_sizes(void) {
               CHECK(defined_host_status(nf4_dequant(NULL, PF(16), PF(16), P(16), K, N, G, dt, NULL)));
               CHECK(defined_host_status(nf4dq_dequant(NULL, PU8(16), PF(16), PF(16), P(16), K, N, G, dt, NULL)));
               CHECK(defined_host_status(nf4_double_quantize(NULL, K, N, G, PU8(16), PF(16), NULL)));
+              CHECK(defined_host_status(w4a16_repack_awq(NULL, PU(16), K, N, G, PU(32), PU(48), NULL)));
               if (d == 0) {
                 CHECK(defined_host_status(w4a16_quantize(NULL, K, N, G, PU(16), P(16), PU(16), NULL)));
                 CHECK(defined_host_status(nf4_quantize(NULL, K, N, G, PF(16), PU(16), PF(16), NULL)));
@@ -96,6 +99,7 @@ int main(void) {
       (fn_t)w4a16_selftest_wait_timeout, (fn_t)w4a16_status_string,
       (fn_t)nf4_default_codebook, (fn_t)nf4dq_gemm,
       (fn_t)nf4dq_dequant,       (fn_t)nf4_double_quantize,
+      (fn_t)w4a16_repack_awq,    (fn_t)w4a16_gemm_silu_mul,
   };
   for (size_t i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i) CHECK(fns[i] != NULL);
 

@@ -237,3 +237,72 @@ def test_nf4dq_one_hot_exact(M):
     X[torch.arange(M), torch.from_numpy(rows)] = 1.0
     Y = w4.nf4dq_gemm(X.cuda(), to_dev_u32(int4.pack_along_k(codes)), to_dev(am_q), to_dev(s2), None)
     assert np.array_equal(bits(Y), nf4.nf4_dequant(codes, am_hat, cb, "bf16")[rows])
+
+
+# ---------------------------------------------------------------- AWQ layout
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("K,N,g", [(1024, 520, 128), (2048, 4104, 64)])
+def test_awq_repack_matches_oracle_and_products(K, N, g, sym):
+    # the same checkpoint in AWQ's layout (codes packed along N in AWQ's
+    # column order) is repacked bit for bit into this library's layout, and
+    # products through it equal the oracle's
+    from oracle import awq
+    W = gaussian_weights(K, N, 0.02, K + N)
+    if sym:
+        q, sc = int4.rtn_quantize_sym(W, g)
+        z = int4.sym_zeros(*sc.shape)
+        qa, za = awq.pack_awq(q), None
+    else:
+        qa, sc, za, q, z = awq.awq_checkpoint(W, g)
+    qw, qz = w4.repack_awq(to_dev_u32(qa), None if za is None else to_dev_u32(za), group_size=g)
+    assert np.array_equal(qw.cpu().numpy().view(np.uint32), int4.pack_along_k(q))
+    if sym:
+        assert qz is None
+    else:
+        assert np.array_equal(qz.cpu().numpy().view(np.uint32), int4.pack_zeros(z))
+    for M in (3, 48):
+        X = activations(M, K, "bf16", M)
+        Y = w4.gemm(X.cuda(), qw, to_dev(sc), qz, group_size=g)
+        torch.cuda.synchronize()
+        Y_ref, A = _expected(q, sc, z, g, "bf16", X)
+        assert_close(to_f64(Y), Y_ref, A, f"AWQ repack K={K} N={N} g={g} sym={sym} M={M}")
+
+
+# ------------------------------------------------- fused SiLU(gate) * up
+@pytest.mark.parametrize("M", [1, 4, 16, 40, 300])
+@pytest.mark.parametrize("g,sym", [(128, False), (64, True)])
+def test_gate_up_silu_mul(M, g, sym):
+    # A = SiLU(X W_gate) * (X W_up) against the oracle's fp64 activation, on
+    # both kernels; F = 776 leaves a ragged last block, K several groups
+    K, F = 1536, 776
+    dtype = "bf16" if M % 2 == 0 else "f16"
+    W = gaussian_weights(K, 2 * F, 0.02, M + g)
+    dev_t, (q, sc, z) = _quantize(W, g, sym)
+    X = activations(M, K, dtype, M)
+    A_ = w4.gemm_silu_mul(X.cuda(), *dev_t[:3], group_size=g)
+    torch.cuda.synchronize()
+    assert A_.shape == (M, F)
+    w_hat = numerics.dtype_bits_to_f64(int4.dequant(q, sc, z, dtype, g), dtype)
+    act, A_ref = product.silu_mul_reference(X.double().numpy(), w_hat)
+    assert_close(to_f64(A_), act, A_ref, f"silu_mul M={M} g={g} sym={sym} {dtype}")
+    # and the same as the unfused product followed by the activation, to
+    # rounding: the two halves are the plain product's columns
+    Y = w4.gemm(X.cuda(), *dev_t[:3], group_size=g).double().cpu()
+    ref2 = (torch.nn.functional.silu(Y[:, :F]) * Y[:, F:]).numpy()
+    assert np.allclose(to_f64(A_), ref2, rtol=3e-2, atol=3e-2 * (np.abs(ref2).max() + 1e-30))
+
+
+def test_gate_up_silu_mul_full_size_decode():
+    # the Qwen2.5-32B-shaped gate_up (5120 -> 2 x 27648) at M = 1, sampled outputs
+    K, F = 5120, 27648
+    W = gaussian_weights(K, 2 * F, 0.02, 11)
+    X = activations(1, K, "bf16", 11)
+    dev_t, _ = _quantize(W, 128, False)
+    A_ = w4.gemm_silu_mul(X.cuda(), *dev_t[:3])
+    torch.cuda.synchronize()
+    cols = np.unique(np.concatenate([np.arange(8), np.arange(F - 8, F),
+                                     np.random.default_rng(3).choice(F, 120, replace=False)]))
+    _, (q, sc, z) = _quantize(W[:, np.concatenate([cols, F + cols])], 128, False)
+    w_hat = numerics.dtype_bits_to_f64(int4.dequant(q, sc, z, "bf16", 128), "bf16")
+    act, A_ref = product.silu_mul_reference(X.double().numpy(), w_hat)
+    assert_close(to_f64(A_)[:, cols], act, A_ref, "silu_mul full size")
