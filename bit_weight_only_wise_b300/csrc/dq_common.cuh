@@ -101,6 +101,19 @@ __device__ __forceinline__ int checked_group(int gr, int G, int* dev_status) {
   return gr;
 }
 
+// ------------------------------------------------- INT4, exact differences
+// The 8 codes of word w as the exact integers (q - z) in fp16, 4 pairs (row
+// j, row j + 4): the 1024 + q / 64 + q forms of dq_word_f16 minus z_lo /
+// z_hi (as in DqConstF16).  Every difference is an integer of at most 4
+// bits, so each subtraction is exact.
+__device__ __forceinline__ void dq_word_codes_f16(uint32_t w, uint32_t z_lo, uint32_t z_hi, uint32_t out[4]) {
+  const uint32_t w8 = w >> 8;
+  out[0] = hsub2_f16(lop3_and_or(w, 0x000F000Fu, 0x64006400u), z_lo);
+  out[1] = hsub2_f16(lop3_and_or(w, 0x00F000F0u, 0x54005400u), z_hi);
+  out[2] = hsub2_f16(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), z_lo);
+  out[3] = hsub2_f16(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), z_hi);
+}
+
 // ---------------------------------------------------------------- INT4, fp16
 // Per-(group, column) constants for the fp16 route; each half of a register
 // may belong to a different (group, column), so act-order can mix them.

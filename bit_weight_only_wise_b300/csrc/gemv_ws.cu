@@ -177,6 +177,22 @@ struct UnitWalk {
   __device__ __forceinline__ int group(int j) const { return GPU == 0 ? gi : GPU == 1 ? kb : kb * GPU + j; }
 };
 
+// The scale-after-sum route: fp16 INT4 whose groups do not split a 16-row
+// MMA step between two scales (every group size but 32).  The weights enter
+// the MMAs as the exact integers q - z and each group's scale multiplies its
+// fp32 partial sum, so a product is sum_g s_g * sum_k x_k (q_k - z): the
+// exact dequantized weight (q - z) * s times x, where the dequantize-then-
+// multiply form uses RNE_fp16((q - z) * s).  The two differ by at most one
+// fp16 rounding of each weight (relative 2^-11), well inside the product
+// tolerance; a one-hot row still gives RNE((q - z) * s) bit for bit (one
+// exact fp32 product, rounded once).  bf16 keeps the dequantize-then-
+// multiply form: there one rounding of each weight (relative 2^-8) is
+// already close to the tolerance on its own.
+template <int FMT, int GPU, bool BF16>
+__host__ __device__ constexpr bool fact_route() {
+  return FMT == kInt4 && GPU <= 2 && !BF16;
+}
+
 // ------------------------------------------------------- act-order pairs
 // One dequantized pair (row j of the word in the low half, row j + 4 in the
 // high half) from the code pair `code` and the zero-point pair `zm`, both in
@@ -362,7 +378,13 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           const uint32_t z = (zw >> (4 * jj)) & 0xFu;
-          if (BF16) {
+          if (fact_route<FMT, GPU, BF16>()) {
+            // scale after the sum: the zero point's code forms and the
+            // scale as fp32
+            k0[jj] = (0x6400u | z) * 0x00010001u;
+            k1[jj] = (0x5400u | (z << 4)) * 0x00010001u;
+            k2[jj] = __float_as_uint(__half2float(__ushort_as_half((unsigned short)(sb[jj] & 0xFFFFu))));
+          } else if (BF16) {
             const DqConstBF16Fma q = dq_const_bf16_fma(z, sb[jj] & 0xFFFFu);
             k0[jj] = __float_as_uint(q.z_lo);
             k1[jj] = __float_as_uint(q.z_hi);
@@ -462,6 +484,7 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
                                             uint64_t* ready, uint64_t* empty, volatile int* abort, int nu, int b0,
                                             int k0, int warp, int lane) {
   using L = WsLayout<NT, FMT, GPU>;
+  constexpr bool FACT = fact_route<FMT, GPU, BF16>();
   const int S = stages_of<NT, FMT, GPU>(a);
   const int gl = lane >> 2, c = lane & 3;
   const uint32_t wbase = smem_u32(smem);
@@ -495,8 +518,13 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
   griddep_launch_dependents();
 
   // two accumulators per (token tile, column pair): even and odd steps o, so
-  // that consecutive MMAs do not wait on each other
-  float acc[NT][2][2][4];
+  // that consecutive MMAs do not wait on each other -- except for two token
+  // tiles on the scale-after-sum route with one group per unit, where the
+  // registers are short and the tiles' MMAs already interleave
+  constexpr int NPAR = FACT && GPU <= 1 && NT == 2 ? 1 : 2;
+  float acc[NT][2][NPAR][4];
+  // FACT: the block's sums so far, each unit's scaled sums added in order
+  float tot[NT][2][4];
   int s = 0;
   uint32_t ph = 0;
   int p0 = -1, p1 = -1;  // split blocks whose tickets are still to be taken
@@ -512,9 +540,15 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
 #pragma unroll
       for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < NPAR; ++h)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[t][r][h][i] = 0.f;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tot[t][r][i] = 0.f;
 #pragma unroll 1
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(&ready[s], ph, abort, a.dev_status, kWaitLimitNs)) return;
@@ -593,8 +627,8 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
             const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-              mma_16816<BF16>(acc[t][rr][o & 1], a0, xv[t][o].x, xv[t][o].y);
-              mma_16816<BF16>(acc[t][rr][o & 1], a1, xv[t][o].z, xv[t][o].w);
+              mma_16816<BF16>(acc[t][rr][(o & 1) % NPAR], a0, xv[t][o].x, xv[t][o].y);
+              mma_16816<BF16>(acc[t][rr][(o & 1) % NPAR], a1, xv[t][o].z, xv[t][o].w);
             }
           }
         } else {
@@ -609,6 +643,12 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
               const uint32_t amv[4] = {am.x, am.y, am.z, am.w};
               dq_word_nf4<BF16>(wd[2 * rr], cbk, __uint_as_float(amv[2 * rr]), pa);
               dq_word_nf4<BF16>(wd[2 * rr + 1], cbk, __uint_as_float(amv[2 * rr + 1]), pb);
+            } else if constexpr (FACT) {
+              const bool second = GPU > 1 && (o & 1);
+              const uint4 e0 = second ? d0 : c0, e1 = second ? d1 : c1;
+              const uint32_t k0v[4] = {e0.x, e0.y, e0.z, e0.w}, k1v[4] = {e1.x, e1.y, e1.z, e1.w};
+              dq_word_codes_f16(wd[2 * rr], k0v[2 * rr], k1v[2 * rr], pa);
+              dq_word_codes_f16(wd[2 * rr + 1], k0v[2 * rr + 1], k1v[2 * rr + 1], pb);
             } else {
               const bool second = GPU > 1 && (o & 1);
               const uint4 e0 = second ? d0 : c0, e1 = second ? d1 : c1, e2 = second ? d2 : c2;
@@ -631,11 +671,42 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
             const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-              mma_16816<BF16>(acc[t][rr][o & 1], a0, xv[t][o].x, xv[t][o].y);
-              mma_16816<BF16>(acc[t][rr][o & 1], a1, xv[t][o].z, xv[t][o].w);
+              // FACT: each unit's sums start from zero (its scales differ
+              // from the previous unit's)
+              float* d = acc[t][rr][(o & 1) % NPAR];
+              if (FACT && o < NPAR)
+                mma_16816_zc<BF16>(d, a0, xv[t][o].x, xv[t][o].y);
+              else
+                mma_16816<BF16>(d, a0, xv[t][o].x, xv[t][o].y);
+              mma_16816<BF16>(d, a1, xv[t][o].z, xv[t][o].w);
             }
           }
         }
+      }
+      if constexpr (FACT) {
+        // the unit's sums times their columns' scales (fp32, exact fp16
+        // values); with two groups per unit, even steps o hold the first
+        // group's rows and odd steps the second's
+        const uint4 sa = c2, sb = GPU == 2 ? d2 : c2;
+        const float s0[4] = {__uint_as_float(sa.x), __uint_as_float(sa.y), __uint_as_float(sa.z),
+                             __uint_as_float(sa.w)};
+        const float s1[4] = {__uint_as_float(sb.x), __uint_as_float(sb.y), __uint_as_float(sb.z),
+                             __uint_as_float(sb.w)};
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int col = 2 * r + (i >> 1);  // this value's column: 4gl + col
+              if (GPU == 2) {
+                tot[t][r][i] = fmaf(s0[col], acc[t][r][0][i], tot[t][r][i]);
+                tot[t][r][i] = fmaf(s1[col], acc[t][r][NPAR - 1][i], tot[t][r][i]);
+              } else {
+                const float v = NPAR == 2 ? acc[t][r][0][i] + acc[t][r][NPAR - 1][i] : acc[t][r][0][i];
+                tot[t][r][i] = fmaf(s0[col], v, tot[t][r][i]);
+              }
+            }
       }
       if (NT != 1) mbar_arrive(&empty[s]);
       if (++s == S) {
@@ -649,7 +720,7 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
 #pragma unroll
       for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) out[t][r][i] = acc[t][r][0][i] + acc[t][r][1][i];
+        for (int i = 0; i < 4; ++i) out[t][r][i] = FACT ? tot[t][r][i] : acc[t][r][0][i] + acc[t][r][NPAR - 1][i];
     if (store_block<NT, BF16>(a, R, (int)blockIdx.x, b0, warp, lane, b, out)) (b == b0 ? p0 : p1) = b;
   }
   finish_blocks<NT, BF16>(a, R, warp, lane, p0, p1);
