@@ -93,10 +93,17 @@ constexpr int kActTableRowBytes = kBN * 4;  // one group: 128 columns x (scale |
 constexpr int kMaxSmem = 227 * 1024;
 
 struct GemmParams {
-  float* partial;  // split-K: fp32 tiles [tile][split][BT][128]
-  int* counters;   // split-K: one ticket per tile
-  int splits;      // K ranges per output tile (1: no split)
+  // Schedule (one CTA per work item, 1-D grid): CTAs [0, dp_tiles) each own
+  // a whole output tile; every later tile is cut into `splits` K ranges of
+  // kb_per_split blocks, one CTA each.  dp_tiles is a whole number of waves
+  // of the SMs, so the split tiles fill what would otherwise be a ragged
+  // last wave.
+  float* partial;  // split tiles: fp32 [tile - dp_tiles][split][BT][128]
+  int* counters;   // split tiles: one ticket per tile
+  int dp_tiles;
+  int splits;      // K ranges per split tile (1: no split tile)
   int kb_per_split;
+  int col_tiles, tok_tiles;
   const int32_t* g_idx;
   const uint16_t* scales;
   const uint32_t* qz;     // nullptr: symmetric (every zero point 8)
@@ -145,12 +152,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // token tiles vary fastest: the CTAs that share a weight tile run together
   // and the weights come from DRAM about once.  Otherwise column tiles vary
   // fastest and the (then L2-resident) weights are shared across a wave.
-  const int w0 = (p.token_fast ? blockIdx.y : blockIdx.x) * p.cpt;  // first weight (and output) column
-  const int m0 = (p.token_fast ? blockIdx.x : blockIdx.y) * p.BT;
-  // Split-K: CTA z of a tile takes K blocks [kb0, kb0 + nkb) (group aligned)
   const int kb_total = (p.K + kBK - 1) / kBK;
-  const int kb0 = (int)blockIdx.z * p.kb_per_split;
-  const int nkb = min(p.kb_per_split, kb_total - kb0);
+  const bool split = (int)blockIdx.x >= p.dp_tiles;
+  const int sj = (int)blockIdx.x - p.dp_tiles;
+  const int tile = split ? p.dp_tiles + sj / p.splits : (int)blockIdx.x;
+  const int tt = tile - p.dp_tiles;       // split tiles: index among them
+  const int zs = split ? sj % p.splits : 0;  // split tiles: which K range
+  const int w0 = (p.token_fast ? tile / p.tok_tiles : tile % p.col_tiles) * p.cpt;  // first weight (and output) column
+  const int m0 = (p.token_fast ? tile % p.tok_tiles : tile / p.col_tiles) * p.BT;
+  // a split tile's CTA zs takes K blocks [kb0, kb0 + nkb) (group aligned)
+  const int kb0 = split ? zs * p.kb_per_split : 0;
+  const int nkb = split ? min(p.kb_per_split, kb_total - kb0) : kb_total;
   volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
@@ -382,13 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     bool emitted = false;
-    if (done && !*abort && p.splits > 1) {
-      // Split-K: this CTA's fp32 tile goes to the workspace; the CTA that
+    if (done && !*abort && split && p.splits > 1) {
+      // Split tile: this CTA's fp32 tile goes to the workspace; the CTA that
       // completes the tile's ticket sums the splits in split order
       // (deterministic) and writes Y.
-      const int tile = (int)(blockIdx.x + gridDim.x * blockIdx.y);
       const size_t tile_floats = (size_t)p.BT * kBN;
-      float* mine = p.partial + ((size_t)tile * p.splits + blockIdx.z) * tile_floats;
+      float* mine = p.partial + ((size_t)tt * p.splits + zs) * tile_floats;
       for (int c = ep * part; c < (ep + 1) * part; c += 8) {
         uint32_t v[8];
         tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
@@ -399,32 +410,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");  // the dequant warps only
       if (dw == 0 && lane == 0) {
         __threadfence();  // release: this CTA's tile is in memory before its ticket moves
-        bars->last = ticket_inc_acquire(p.counters + tile, (uint32_t)(p.splits - 1)) == (uint32_t)(p.splits - 1);
+        bars->last = ticket_inc_acquire(p.counters + tt, (uint32_t)(p.splits - 1)) == (uint32_t)(p.splits - 1);
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
-      if (bars->last && (ok || p.silu)) {
-        const float* base = p.partial + (size_t)tile * p.splits * tile_floats;
-        for (int c = ep * part; c < (ep + 1) * part; c += 8) {
-          float acc[8];
+      if (bars->last) {
+        // The tile's sum, 16 bytes per load: float4 f of the tile is token
+        // f / 32, lanes 4 (f % 32) .. +3; each value adds the splits in split
+        // order (the same order for every element, whichever CTA sums).
+        // Several float4s per thread keep enough loads in flight to cover
+        // the L2 latency.
+        const float4* base = reinterpret_cast<const float4*>(p.partial + (size_t)tt * p.splits * tile_floats);
+        const int tid = (int)threadIdx.x - 64;  // the dequant warps
+        const int nf = p.BT * (kBN / 4);
+        const size_t zstride = tile_floats / 4;
+        constexpr int kU = 4;
+        for (int f0 = tid; f0 < nf; f0 += kU * kDqWarps * 32) {
+          float4 acc[kU];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-          // four splits' loads in flight per round trip, summed in split order
-          for (int z0 = 0; z0 < p.splits; z0 += 4) {
-            float v[4][8];
+          for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int z = 0; z < p.splits; ++z) {
+            float4 v[kU];
 #pragma unroll
-            for (int zz = 0; zz < 4; ++zz)
+            for (int u = 0; u < kU; ++u) {
+              const int f = f0 + u * kDqWarps * 32;
+              v[u] = f < nf ? __ldcg(base + (size_t)z * zstride + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                v[zz][j] = z0 + zz < p.splits
-                               ? __ldcg(base + (size_t)(z0 + zz) * tile_floats + (size_t)(c + j) * kBN + nl)
-                               : 0.f;
-#pragma unroll
-            for (int zz = 0; zz < 4; ++zz)
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                if (z0 + zz < p.splits) acc[j] += v[zz][j];
+            for (int u = 0; u < kU; ++u) {
+              acc[u].x += v[u].x;
+              acc[u].y += v[u].y;
+              acc[u].z += v[u].z;
+              acc[u].w += v[u].w;
+            }
           }
-          emit(c, acc);
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int f = f0 + u * kDqWarps * 32;
+            if (f >= nf) continue;
+            const int t = f / (kBN / 4), l0 = 4 * (f % (kBN / 4));
+            const float vv[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+            if (p.silu) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) xb[(size_t)t * kBN + l0 + q] = vv[q];
+            } else if (m0 + t < p.M) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int l = l0 + q;
+                const int oc = w0 + (l >> 6) * p.hi2 + (l & 63);
+                if (oc < p.Nout) p.Y[(size_t)(m0 + t) * p.ldy + oc] = (uint16_t)(pack2_rn(vv[q], 0.f, BF16) & 0xFFFFu);
+              }
+            }
+          }
         }
       }
       emitted = bars->last != 0;
@@ -464,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ host side
 template <int FMT, bool BF16>
-cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const GemmParams& p, dim3 grid,
+cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const GemmParams& p, unsigned grid,
                       cudaStream_t st) {
   static std::atomic<unsigned long long> attr_done{0};
   unsigned long long dev_bit = 0;
@@ -482,15 +518,19 @@ cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const Gemm
 
 }  // namespace
 
-// Split-K plan: when the output tiles do not fill one wave of the SMs, each
-// tile's K range is cut into `splits` group-aligned parts, as many as keep
-// every part's CTA in the first wave and every part at least 8 K blocks long.
+// Schedule: the output tiles run as whole tiles in full waves of the SMs;
+// the R tiles left over for a last, ragged wave (all of them when they do
+// not fill one wave) are cut along K into `splits` group-aligned parts, as
+// many as keep every part's CTA in that wave and every part at least 8 K
+// blocks long -- so the last wave is short instead of ragged.  Only those
+// R tiles pay for fp32 partial tiles and a ticket.
 GemmSplit gemm_split_plan(int M, int N, int K, bool act_order) {
   GemmSplit sp{};
   sp.BT = gemm_tokens_per_cta(M, act_order);
   const int tiles = ((N + kBN - 1) / kBN) * ((M + sp.BT - 1) / sp.BT);
   const int kb_total = (K + kBK - 1) / kBK;
-  int splits = tiles > 0 ? kNumSMs / tiles : 1;
+  const int rest = tiles % kNumSMs;
+  int splits = rest > 0 ? kNumSMs / rest : 1;
   if (splits > kb_total / 8) splits = kb_total / 8;
   if (splits < 1) splits = 1;
   int kb_per = (kb_total + splits - 1) / splits;
@@ -498,8 +538,9 @@ GemmSplit gemm_split_plan(int M, int N, int K, bool act_order) {
   sp.splits = (kb_total + kb_per - 1) / kb_per;
   sp.kb_per_split = kb_per;
   sp.tiles = tiles;
+  sp.dp_tiles = sp.splits > 1 ? tiles - rest : tiles;
   sp.workspace_bytes =
-      sp.splits > 1 ? kCountersBytes + (size_t)tiles * sp.splits * sp.BT * kBN * sizeof(float) : 0;
+      sp.splits > 1 ? kCountersBytes + (size_t)rest * sp.splits * sp.BT * kBN * sizeof(float) : 0;
   return sp;
 }
 
@@ -552,6 +593,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   p.BT = BT;
   p.idesc = sm100::idesc_f16(bf16, kBN, BT);
   const GemmSplit sp = gemm_split_plan(a.M, a.N, a.K, act);
+  p.dp_tiles = sp.dp_tiles;
   p.splits = sp.splits;
   p.kb_per_split = sp.kb_per_split;
   if (sp.splits > 1) {
@@ -564,9 +606,11 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   p.hiofs = a.silu ? a.N / 2 : kBN / 2;
   p.hi2 = a.silu ? 0 : kBN / 2;
   p.Nout = p.ldy = a.silu ? a.N / 2 : a.N;
-  const unsigned col_tiles = (p.Nout + p.cpt - 1) / p.cpt, tok_tiles = (a.M + BT - 1) / BT;
+  p.col_tiles = (p.Nout + p.cpt - 1) / p.cpt;
+  p.tok_tiles = (a.M + BT - 1) / BT;
+  if (p.col_tiles * p.tok_tiles != sp.tiles) return cudaErrorInvalidValue;
   p.token_fast = (size_t)a.K * a.N / 2 > (size_t)64 << 20;
-  dim3 grid = p.token_fast ? dim3(tok_tiles, col_tiles, sp.splits) : dim3(col_tiles, tok_tiles, sp.splits);
+  const unsigned grid = (unsigned)(sp.dp_tiles + (sp.tiles - sp.dp_tiles) * sp.splits);
   if (nf4) return bf16 ? launch_tc<kFmtNF4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtNF4, false>(tmX, tmW, p, grid, st);
   if (act)
     return bf16 ? launch_tc<kFmtInt4Act, true>(tmX, tmW, p, grid, st)

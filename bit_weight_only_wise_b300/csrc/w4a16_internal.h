@@ -127,6 +127,7 @@ int gemm_tokens_per_cta(int M, bool act_order);
 struct GemmSplit {
   int BT;
   int tiles;
+  int dp_tiles;  // tiles run whole, in full waves; the rest are split along K
   int splits;
   int kb_per_split;
   size_t workspace_bytes;  // 0 when not split
