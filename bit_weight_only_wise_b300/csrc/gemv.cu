@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
 
   int p0 = -1, p1 = -1;  // split blocks whose tickets are still to be taken
   auto flush = [&](int b) {
-    if (store_block<NT, BF16>(a, R, cta, first_block, warp, lane, b, acc)) (b == first_block ? p0 : p1) = b;
+    if (store_block<NT, BF16, false>(a, R, cta, first_block, warp, lane, b, acc)) (b == first_block ? p0 : p1) = b;
   };
 
   // lane-invariant parts of the shared-memory and activation addresses
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_ctas_per_sm(NT == 1 ? 1 : 1
     g = gn;
   }
   if (cur_b >= 0) flush(cur_b);
-  finish_blocks<NT, BF16>(a, R, warp, lane, p0, p1);
+  finish_blocks<NT, BF16, false>(a, R, warp, lane, p0, p1);
 }
 
 template <int NT, int FMT, bool BF16>

@@ -35,9 +35,25 @@ struct Range {
 // SiLU(g) * u in fp32, the gate_up epilogue
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
 
+// A launch's column geometry (see GemvArgs), fixed at compile time for the
+// plain product -- 256-column blocks, halves 128 columns apart, Y as wide as
+// N -- and read from the arguments for the fused SiLU epilogue, which is a
+// kernel variant of its own: the plain kernels carry none of its code or
+// registers (the 32-row-group bf16 variant's spills went from 152 to 12
+// bytes).
+template <bool SILU>
+struct Geom {
+  __device__ __forceinline__ static int cpb(const GemvArgs& a) { return SILU ? a.cpb : kGemvCols; }
+  __device__ __forceinline__ static int hiofs(const GemvArgs& a) { return SILU ? a.hiofs : kGemvCols / 2; }
+  __device__ __forceinline__ static int hi2(const GemvArgs& a) { return SILU ? a.hi2 : kGemvCols / 2; }
+  __device__ __forceinline__ static int nout(const GemvArgs& a) { return SILU ? a.Nout : a.N; }
+  __device__ __forceinline__ static int ldy(const GemvArgs& a) { return SILU ? a.ldy : a.N; }
+};
+
 // first output column of warp w's slice of block b
+template <bool SILU>
 __device__ __forceinline__ int slice_col(const GemvArgs& a, int b, int warp) {
-  return b * a.cpb + 32 * (warp & 3) + (warp >> 2) * a.hi2;
+  return b * Geom<SILU>::cpb(a) + 32 * (warp & 3) + (warp >> 2) * Geom<SILU>::hi2(a);
 }
 
 template <bool BF16>
@@ -129,30 +145,32 @@ __device__ __forceinline__ float* slice_slot(const GemvArgs& a, int cta, int seg
 // Fused SiLU, whole block: both halves pass through the CTA's exchange slot,
 // a barrier of the consumer warps (named barrier 1, all kSliceWarps warps)
 // orders the writes before the gate warps read.
-template <int NT, bool BF16>
+template <int NT, bool BF16, bool SILU>
 __device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, int cta, int first_block, int warp,
                                             int lane, int b, const float (&acc)[NT][2][4]) {
   const int gl = lane >> 2, c = lane & 3;
-  const int col0 = slice_col(a, b, warp) + 4 * gl;
+  using G = Geom<SILU>;
+  const int col0 = slice_col<SILU>(a, b, warp) + 4 * gl;
   const int i_first = R.owner((long long)b * a.KB);
   const int i_last = R.owner((long long)(b + 1) * a.KB - 1);
-  if (i_first == i_last && a.silu) {
+  if (SILU && i_first == i_last) {
     float* xs = slice_slot(a, kNumSMs * 2 + cta / 2, cta % 2, 0);
     store_slot<NT>(a, xs + (size_t)warp * a.M * 32, lane, acc);
     asm volatile("bar.sync 1, %0;" ::"r"(kSliceWarps * 32) : "memory");
     if (warp < kSliceWarps / 2) {
-      const int col = slice_col(a, b, warp) + lane;
+      const int col = slice_col<SILU>(a, b, warp) + lane;
       const float* gp = xs + (size_t)warp * a.M * 32 + lane;
       const float* up = xs + (size_t)(warp + kSliceWarps / 2) * a.M * 32 + lane;
-      if (col < a.Nout)
+      if (col < G::nout(a))
         for (int t = 0; t < a.M; ++t)
-          a.Y[(size_t)t * a.ldy + col] = (uint16_t)(pack2_rn(silu_mul(gp[t * 32], up[t * 32]), 0.f, BF16) & 0xFFFFu);
+          a.Y[(size_t)t * G::ldy(a) + col] =
+              (uint16_t)(pack2_rn(silu_mul(gp[t * 32], up[t * 32]), 0.f, BF16) & 0xFFFFu);
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kSliceWarps * 32) : "memory");  // the slot is free again
     return false;
   }
   if (i_first == i_last) {
-    if (col0 >= a.Nout) return false;
+    if (col0 >= G::nout(a)) return false;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -160,9 +178,9 @@ __device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, i
         const int tok = 8 * t + 2 * c;
         const int col = col0 + 2 * r;
         if (tok < a.M)
-          *reinterpret_cast<uint32_t*>(a.Y + (size_t)tok * a.ldy + col) = pack2_rn(acc[t][r][0], acc[t][r][2], BF16);
+          *reinterpret_cast<uint32_t*>(a.Y + (size_t)tok * G::ldy(a) + col) = pack2_rn(acc[t][r][0], acc[t][r][2], BF16);
         if (tok + 1 < a.M)
-          *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * a.ldy + col) =
+          *reinterpret_cast<uint32_t*>(a.Y + (size_t)(tok + 1) * G::ldy(a) + col) =
               pack2_rn(acc[t][r][1], acc[t][r][3], BF16);
       }
     return false;
@@ -176,10 +194,11 @@ __device__ __forceinline__ bool store_block(const GemvArgs& a, const Range& R, i
 // once and write Y.  Contributor i wrote the block as its first block (slot 0)
 // unless its range starts before the block, which only the first contributor's
 // can.  Several contributors' loads are in flight at once.
-template <int NT, bool BF16>
+template <int NT, bool BF16, bool SILU>
 __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, int warp, int lane, int b) {
-  const int col = slice_col(a, b, warp) + lane;
-  if (col >= a.Nout) return;
+  using G = Geom<SILU>;
+  const int col = slice_col<SILU>(a, b, warp) + lane;
+  if (col >= G::nout(a)) return;
   const int i_first = R.owner((long long)b * a.KB);
   const int i_last = R.owner((long long)(b + 1) * a.KB - 1);
   const int sg_first = R.start(i_first) == (long long)b * a.KB ? 0 : 1;
@@ -187,14 +206,14 @@ __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, 
   auto slot = [&](int i) -> const float* {
     return a.partial + ((size_t)(i * 2 + (i == i_first ? sg_first : 0)) * kSliceWarps + warp) * stride + lane;
   };
-  if (a.silu) {  // slices warp (gate) and warp + 4 (up), both summed in contributor order
+  if (SILU) {  // slices warp (gate) and warp + 4 (up), both summed in contributor order
     for (int t = 0; t < a.M; ++t) {
       float g = 0.f, u = 0.f;
       for (int i = i_first; i <= i_last; ++i) {
         g += __ldcg(slot(i) + t * 32);
         u += __ldcg(slot(i) + (size_t)(kSliceWarps / 2) * stride + t * 32);
       }
-      a.Y[(size_t)t * a.ldy + col] = (uint16_t)(pack2_rn(silu_mul(g, u), 0.f, BF16) & 0xFFFFu);
+      a.Y[(size_t)t * G::ldy(a) + col] = (uint16_t)(pack2_rn(silu_mul(g, u), 0.f, BF16) & 0xFFFFu);
     }
     return;
   }
@@ -230,11 +249,12 @@ __device__ __forceinline__ void reduce_block(const GemvArgs& a, const Range& R, 
   }
 #pragma unroll
   for (int t = 0; t < 8 * NT; ++t)
-    if (t < a.M) a.Y[(size_t)t * a.ldy + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
+    if (t < a.M) a.Y[(size_t)t * G::ldy(a) + col] = (uint16_t)(pack2_rn(sum[t], 0.f, BF16) & 0xFFFFu);
 }
 
 // reduce_block for two blocks at M = 1 with every contributor's load of both
-// in flight at once (a warp that completes both of its blocks' counts)
+// in flight at once (a warp that completes both of its blocks' counts; the
+// plain product only)
 template <bool BF16>
 __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Range& R, int warp, int lane, int b0,
                                                      int b1) {
@@ -245,7 +265,7 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
     first[h] = R.owner((long long)bs[h] * a.KB);
     last[h] = R.owner((long long)(bs[h] + 1) * a.KB - 1);
     sgf[h] = R.start(first[h]) == (long long)bs[h] * a.KB ? 0 : 1;
-    col[h] = slice_col(a, bs[h], warp) + lane;
+    col[h] = slice_col<false>(a, bs[h], warp) + lane;
   }
   float sum[2] = {0.f, 0.f};
   const int n = max(last[0] - first[0], last[1] - first[1]) + 1;
@@ -258,7 +278,7 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
         const int i = first[h] + j0 + j;
         const float* pp =
             a.partial + ((size_t)(i * 2 + (i == first[h] ? sgf[h] : 0)) * kSliceWarps + warp) * 32 + lane;
-        v[h][j] = (i <= last[h] && col[h] < a.Nout) ? __ldcg(pp) : 0.f;
+        v[h][j] = (i <= last[h] && col[h] < a.N) ? __ldcg(pp) : 0.f;
       }
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -267,13 +287,13 @@ __device__ __forceinline__ void reduce_two_blocks_m1(const GemvArgs& a, const Ra
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h)
-    if (col[h] < a.Nout) a.Y[col[h]] = (uint16_t)(pack2_rn(sum[h], 0.f, BF16) & 0xFFFFu);
+    if (col[h] < a.N) a.Y[col[h]] = (uint16_t)(pack2_rn(sum[h], 0.f, BF16) & 0xFFFFu);
 }
 
 // The CTA is done: publish this warp's partials of split blocks p0 and p1
 // (the CTA's first and last block; -1 for none) and take their tickets; the
 // contributor that completes a block's count sums it.
-template <int NT, bool BF16>
+template <int NT, bool BF16, bool SILU>
 __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R, int warp, int lane, int p0, int p1) {
   if (p0 < 0 && p1 < 0) return;
   // the warp barrier orders every lane's partial stores before lane 0's
@@ -286,32 +306,32 @@ __device__ __forceinline__ void finish_blocks(const GemvArgs& a, const Range& R,
   int last0 = 0, last1 = 0;
   if (lane == 0) {
     __threadfence();
-    const int tw = a.silu ? (warp & (kSliceWarps / 2 - 1)) : warp;
+    const int tw = SILU ? (warp & (kSliceWarps / 2 - 1)) : warp;
     if (p0 >= 0) {
       uint32_t w = (uint32_t)(R.owner((long long)(p0 + 1) * a.KB - 1) - R.owner((long long)p0 * a.KB));
-      if (a.silu) w = 2 * w + 1;
+      if (SILU) w = 2 * w + 1;
       last0 = sm100::ticket_inc_acquire(a.counters + p0 * kSliceWarps + tw, w) == w;
     }
     if (p1 >= 0) {
       uint32_t w = (uint32_t)(R.owner((long long)(p1 + 1) * a.KB - 1) - R.owner((long long)p1 * a.KB));
-      if (a.silu) w = 2 * w + 1;
+      if (SILU) w = 2 * w + 1;
       last1 = sm100::ticket_inc_acquire(a.counters + p1 * kSliceWarps + tw, w) == w;
     }
   }
   __syncwarp();
   last0 = __shfl_sync(0xFFFFFFFFu, last0, 0);
   last1 = __shfl_sync(0xFFFFFFFFu, last1, 0);
-  if (a.silu) {  // the completing warp may be the gate or the up one: sum from the gate slice
-    if (last0) reduce_block<NT, BF16>(a, R, warp & (kSliceWarps / 2 - 1), lane, p0);
-    if (last1) reduce_block<NT, BF16>(a, R, warp & (kSliceWarps / 2 - 1), lane, p1);
+  if (SILU) {  // the completing warp may be the gate or the up one: sum from the gate slice
+    if (last0) reduce_block<NT, BF16, SILU>(a, R, warp & (kSliceWarps / 2 - 1), lane, p0);
+    if (last1) reduce_block<NT, BF16, SILU>(a, R, warp & (kSliceWarps / 2 - 1), lane, p1);
     return;
   }
   if (last0 && last1 && a.M == 1) {  // both blocks: one round trip for the two
     reduce_two_blocks_m1<BF16>(a, R, warp, lane, p0, p1);
     return;
   }
-  if (last0) reduce_block<NT, BF16>(a, R, warp, lane, p0);
-  if (last1) reduce_block<NT, BF16>(a, R, warp, lane, p1);
+  if (last0) reduce_block<NT, BF16, SILU>(a, R, warp, lane, p0);
+  if (last1) reduce_block<NT, BF16, SILU>(a, R, warp, lane, p1);
 }
 
 }  // namespace w4a16

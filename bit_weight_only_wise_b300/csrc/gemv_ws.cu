@@ -224,7 +224,7 @@ __device__ __forceinline__ uint32_t dq_pair_rows(uint32_t code, uint32_t zm, uin
 }
 
 // ------------------------------------------------------------------ roles
-template <int NT, int FMT, int GPU>
+template <int NT, int FMT, int GPU, bool SILU>
 __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmA,
                                             const GemvArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                             volatile int* abort, int nu, int b0, int k0, int lane) {
@@ -238,10 +238,12 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   // unit's second half starts a.hiofs weight columns and a.hi2 output
   // columns after its first): its weight box (lanes < 8), its 8 scales, their
   // output column, and their zero word
-  const int wcol_l = 32 * (lane & 3) + (lane >> 2) * a.hiofs;
-  const int scol_l = 8 * (lane & 15) + (lane >> 4) * a.hiofs;
-  const int ocol_l = 8 * (lane & 15) + (lane >> 4) * a.hi2;
-  const int zw_l = (lane >> 4) * (a.hiofs >> 3) + (lane & 15);
+  using G = Geom<SILU>;
+  const int cpb = G::cpb(a);
+  const int wcol_l = 32 * (lane & 3) + (lane >> 2) * G::hiofs(a);
+  const int scol_l = 8 * (lane & 15) + (lane >> 4) * G::hiofs(a);
+  const int ocol_l = 8 * (lane & 15) + (lane >> 4) * G::hi2(a);
+  const int zw_l = (lane >> 4) * (G::hiofs(a) >> 3) + (lane & 15);
   // the unit's metadata into stage s, by cp.async (NF4's absmax by TMA)
   auto issue_meta = [&](int s, const UnitWalk<GPU>& u) {
     const uint32_t side = side0 + s * L::SIDE;
@@ -251,13 +253,13 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
       for (int j = 0; j < L::NGRP; ++j) {
         const int gi = u.group(j);
         const bool gv = GPU <= 1 || gi < a.NG;  // only 32/64-row groups can run past K
-        const int col = b * a.cpb + scol_l;
-        const bool sv = gv && b * a.cpb + ocol_l < a.Nout;
+        const int col = b * cpb + scol_l;
+        const bool sv = gv && b * cpb + ocol_l < G::nout(a);
         cp_async_16(side + L::RAW + j * (kGemvCols * 2) + 16 * lane, sv ? a.scales + (size_t)gi * a.N + col : a.scales,
                     sv);
         // symmetric weights: a.nwz = 0, so the zero words are zero-filled
         // (the helper turns them into 8s)
-        const int zc = b * (a.cpb >> 3) + zw_l;
+        const int zc = b * (cpb >> 3) + zw_l;
         const bool zv = sv && zc < a.nwz;
         cp_async_4(side + L::RAW + L::NGRP * (kGemvCols * 2) + j * 128 + 4 * lane,
                    zv ? a.qz + (size_t)gi * nw + zc : a.qw, zv);
@@ -292,7 +294,7 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
     if (lane == 0) mbar_arrive_expect_tx(&full[s], L::TX);
     __syncwarp();
     if (lane < kCW)
-      tma_load_2d(smem + s * kWBytes + lane * kWBox, tmW, &full[s], u.b * a.cpb + wcol_l, u.kb * 16);
+      tma_load_2d(smem + s * kWBytes + lane * kWBox, tmW, &full[s], u.b * cpb + wcol_l, u.kb * 16);
     if (lane == 0) tma_load_2d(smem + S * kWBytes + s * L::SIDE + L::X, tmX, &full[s], u.kb * 128, 0);
     issue_meta(s, u);
   };
@@ -309,14 +311,14 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   {
     UnitWalk<GPU> u(a, b0, k0);
     for (int k = 0; k < n_first; ++k) {
-      if (lane < kCW) tma_prefetch_l2_2d(tmW, u.b * a.cpb + wcol_l, u.kb * 16);
+      if (lane < kCW) tma_prefetch_l2_2d(tmW, u.b * cpb + wcol_l, u.kb * 16);
       if constexpr (FMT == kInt4) {
-        const int col = u.b * a.cpb + scol_l;
+        const int col = u.b * cpb + scol_l;
 #pragma unroll
         for (int j = 0; j < L::NGRP; ++j) {
           const int gi = u.group(j);
-          if (gi < a.NG && u.b * a.cpb + ocol_l < a.Nout) prefetch_l2(a.scales + (size_t)gi * a.N + col);
-          if (gi < a.NG && a.nwz && (lane & 15) == 0) prefetch_l2(a.qz + (size_t)gi * nw + u.b * (a.cpb >> 3) + zw_l);
+          if (gi < a.NG && u.b * cpb + ocol_l < G::nout(a)) prefetch_l2(a.scales + (size_t)gi * a.N + col);
+          if (gi < a.NG && a.nwz && (lane & 15) == 0) prefetch_l2(a.qz + (size_t)gi * nw + u.b * (cpb >> 3) + zw_l);
         }
       } else if constexpr (FMT == kNF4) {
         if (lane == kCW) tma_prefetch_l2_2d(tmA, u.b * kGemvCols, u.kb * 2);
@@ -479,7 +481,7 @@ __device__ __forceinline__ void act_table_load(const GemvArgs& a, uint32_t tab, 
   consumers_sync();
 }
 
-template <int NT, int FMT, bool BF16, int GPU>
+template <int NT, int FMT, bool BF16, int GPU, bool SILU>
 __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, uint8_t* smem, const float* cbk,
                                             uint64_t* ready, uint64_t* empty, volatile int* abort, int nu, int b0,
                                             int k0, int warp, int lane) {
@@ -721,12 +723,12 @@ __device__ __forceinline__ void ws_consumer(const GemvArgs& a, const Range& R, u
       for (int r = 0; r < 2; ++r)
 #pragma unroll
         for (int i = 0; i < 4; ++i) out[t][r][i] = FACT ? tot[t][r][i] : acc[t][r][0][i] + acc[t][r][NPAR - 1][i];
-    if (store_block<NT, BF16>(a, R, (int)blockIdx.x, b0, warp, lane, b, out)) (b == b0 ? p0 : p1) = b;
+    if (store_block<NT, BF16, SILU>(a, R, (int)blockIdx.x, b0, warp, lane, b, out)) (b == b0 ? p0 : p1) = b;
   }
-  finish_blocks<NT, BF16>(a, R, warp, lane, p0, p1);
+  finish_blocks<NT, BF16, SILU>(a, R, warp, lane, p0, p1);
 }
 
-template <int NT, int FMT, bool BF16, int GPU>
+template <int NT, int FMT, bool BF16, int GPU, bool SILU>
 __global__ void __launch_bounds__(kWsThreads, FMT == kInt4Act ? 1 : 2)
     gemv_ws_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmA, const GemvArgs a) {
@@ -759,11 +761,11 @@ __global__ void __launch_bounds__(kWsThreads, FMT == kInt4Act ? 1 : 2)
   __syncthreads();
   volatile int* abort = &abort_flag;
   if (warp == kProducer)
-    ws_producer<NT, FMT, GPU>(&tmW, &tmX, &tmA, a, smem, full, empty, abort, nu, b0, k0, lane);
+    ws_producer<NT, FMT, GPU, SILU>(&tmW, &tmX, &tmA, a, smem, full, empty, abort, nu, b0, k0, lane);
   else if (warp == kHelper)
     ws_helper<NT, FMT, BF16, GPU>(a, smem, full, ready, abort, nu, lane);
   else
-    ws_consumer<NT, FMT, BF16, GPU>(a, R, smem, s_cb, ready, empty, abort, nu, b0, k0, warp, lane);
+    ws_consumer<NT, FMT, BF16, GPU, SILU>(a, R, smem, s_cb, ready, empty, abort, nu, b0, k0, warp, lane);
 }
 
 // Pipeline depth and CTAs per SM of a launch.  Act-order: its consumers hold
@@ -788,7 +790,7 @@ bool ws_shape(int NG, int* stages, int* ctas_per_sm, int* smem) {
   return true;
 }
 
-template <int NT, int FMT, bool BF16, int GPU>
+template <int NT, int FMT, bool BF16, int GPU, bool SILU>
 cudaError_t launch_ws(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemvArgs& a0, cudaStream_t st) {
   GemvArgs a = a0;
   int stages = 0, cps = 0, smem = 0;
@@ -815,10 +817,10 @@ cudaError_t launch_ws(const CUtensorMap& tmW, const CUtensorMap& tmA, const Gemv
   static std::atomic<unsigned long long> attr_done{0};
   unsigned long long dev_bit = 0;
   if (attrs_pending(attr_done, &dev_bit)) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16, GPU>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16, GPU, SILU>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kOneCtaSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16, GPU>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(gemv_ws_kernel<NT, FMT, BF16, GPU, SILU>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(dev_bit, std::memory_order_release);
@@ -833,15 +835,29 @@ cudaError_t launch_ws(const CUtensorMap& tmW, const CUtensorMap& tmA, const Gemv
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_ws_kernel<NT, FMT, BF16, GPU>, tmW, tmX, tmA, a);
+  return cudaLaunchKernelEx(&cfg, gemv_ws_kernel<NT, FMT, BF16, GPU, SILU>, tmW, tmX, tmA, a);
 }
 
+template <int FMT, int GPU, bool SILU>
+cudaError_t launch_fmt_s(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemvArgs& a, bool bf16,
+                         cudaStream_t st) {
+  if (a.M <= 8)
+    return bf16 ? launch_ws<1, FMT, true, GPU, SILU>(tmW, tmA, a, st)
+                : launch_ws<1, FMT, false, GPU, SILU>(tmW, tmA, a, st);
+  return bf16 ? launch_ws<2, FMT, true, GPU, SILU>(tmW, tmA, a, st)
+              : launch_ws<2, FMT, false, GPU, SILU>(tmW, tmA, a, st);
+}
+
+// the fused SiLU epilogue exists for plain INT4 groups only
 template <int FMT, int GPU>
 cudaError_t launch_fmt(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemvArgs& a, bool bf16,
                        cudaStream_t st) {
-  if (a.M <= 8)
-    return bf16 ? launch_ws<1, FMT, true, GPU>(tmW, tmA, a, st) : launch_ws<1, FMT, false, GPU>(tmW, tmA, a, st);
-  return bf16 ? launch_ws<2, FMT, true, GPU>(tmW, tmA, a, st) : launch_ws<2, FMT, false, GPU>(tmW, tmA, a, st);
+  if constexpr (FMT == kInt4) {
+    if (a.silu) return launch_fmt_s<FMT, GPU, true>(tmW, tmA, a, bf16, st);
+  } else {
+    if (a.silu) return cudaErrorInvalidValue;
+  }
+  return launch_fmt_s<FMT, GPU, false>(tmW, tmA, a, bf16, st);
 }
 
 bool encode_weights(CUtensorMap* tmW, const GemvArgs& a) {
