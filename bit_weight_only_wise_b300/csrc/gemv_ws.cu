@@ -239,6 +239,10 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   // columns after its first): its weight box (lanes < 8), its 8 scales, their
   // output column, and their zero word
   using G = Geom<SILU>;
+  // every weight byte is read once per call: stream them evict-first, so
+  // that they do not push the activations, partial sums and tickets, or the
+  // next launch's data, out of L2 (1.9% on the decode stack)
+  const uint64_t wpol = l2_evict_first_policy();
   const int cpb = G::cpb(a);
   const int wcol_l = 32 * (lane & 3) + (lane >> 2) * G::hiofs(a);
   const int scol_l = 8 * (lane & 15) + (lane >> 4) * G::hiofs(a);
@@ -294,7 +298,7 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
     if (lane == 0) mbar_arrive_expect_tx(&full[s], L::TX);
     __syncwarp();
     if (lane < kCW)
-      tma_load_2d(smem + s * kWBytes + lane * kWBox, tmW, &full[s], u.b * cpb + wcol_l, u.kb * 16);
+      tma_load_2d_hint(smem + s * kWBytes + lane * kWBox, tmW, &full[s], u.b * cpb + wcol_l, u.kb * 16, wpol);
     if (lane == 0) tma_load_2d(smem + S * kWBytes + s * L::SIDE + L::X, tmX, &full[s], u.kb * 128, 0);
     issue_meta(s, u);
   };
