@@ -108,8 +108,10 @@ typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype;
 /*
  * Y = X . W_hat for the INT4 format, any M >= 0.  Dispatches on M: M <= 16
  * runs the split-K decode kernel (as w4a16_gemv), larger M the tcgen05
- * tensor-core kernel, which also splits K when its output tiles alone would
- * leave SMs idle (fp32 partial tiles summed in a fixed order: deterministic).
+ * tensor-core kernel: output tiles of 128 columns x up to 256 tokens run
+ * whole in full waves of the SMs, and the tiles left over for a ragged last
+ * wave (all tiles, when they do not fill one wave) are split along K (fp32
+ * partial tiles summed in a fixed order: deterministic).
  *   group_size: 32, 64, a multiple of 128, or K; others W4A16_ERR_UNSUPPORTED.
  *   qzeros: NULL for symmetric weights.
  *   g_idx with M > 16: the tensor-core kernel keeps every group's (scale,
@@ -268,7 +270,11 @@ w4a16_status nf4_double_quantize(const float* absmax, int K, int N, int blocksiz
 
 /* Bytes of workspace w4a16_gemm / w4a16_gemv / nf4_gemm need for this
  * shape (0 when none is needed, and for shapes outside the size limits,
- * which those calls reject).  Pure host function. */
+ * which those calls reject).  Pure host function.  For M > 16: the ticket
+ * area (128 KiB) plus one fp32 partial tile (128 columns x BT tokens) per
+ * K part of each leftover tile, where BT = min(round_up(M, 32), 256) (128
+ * with g_idx), rest = tiles mod 148, parts = min(148 / rest, (K / 64) / 8)
+ * rounded to group-aligned ranges; 0 when no tile is split. */
 size_t w4a16_workspace_bytes(int M, int N, int K);
 
 /*

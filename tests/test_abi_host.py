@@ -129,6 +129,39 @@ def test_workspace_sizes_are_pure_and_bounded(lib):
             assert b <= 64 * 1024 * 1024
 
 
+def _prefill_plan_bytes(M, N, K, act):
+    # the tensor-core kernel's schedule as w4a16.h documents it beside
+    # w4a16_workspace_bytes: tiles of 128 columns x BT tokens run whole in full waves of
+    # the 148 SMs; the tiles left over for a ragged last wave (all of them
+    # below one wave) are cut along K into splits = min(148 // rest, K blocks
+    # / 8) group-aligned parts, each with an fp32 partial tile
+    cap = 128 if act else 256
+    BT = cap if M >= cap else (M + 31) // 32 * 32
+    tiles = -(-N // 128) * -(-M // BT)
+    kb = -(-K // 64)
+    rest = tiles % 148
+    splits = max(1, min(148 // rest if rest else 1, kb // 8))
+    per = -(-kb // splits)
+    per += per & 1
+    splits = -(-kb // per)
+    if splits <= 1:
+        return 0
+    return 4096 * 8 * 4 + rest * splits * BT * 128 * 4
+
+
+def test_prefill_schedule_workspace(lib):
+    # the prefill workspace is the ticket area plus one fp32 partial tile per
+    # part of each leftover tile, whichever of the plain and act-order plans
+    # needs more
+    for M, N, K in ((17, 150 * 128, 1024), (1024, 5120, 5120), (256, 5120, 5120), (1024, 5120, 27648),
+                    (4096, 55296, 5120), (4096, 5120, 5120), (64, 8192, 8192), (300, 520, 768)):
+        want = max(_prefill_plan_bytes(M, N, K, False), _prefill_plan_bytes(M, N, K, True))
+        assert lib.w4a16_workspace_bytes(M, N, K) == want, (M, N, K)
+    # one full wave and no leftover: no partial tiles
+    assert lib.w4a16_workspace_bytes(256, 148 * 128, 4096) == _prefill_plan_bytes(256, 148 * 128, 4096, True)
+    assert _prefill_plan_bytes(256, 148 * 128, 4096, False) == 0
+
+
 def test_noalloc_scratch_fits_every_decode_call(lib):
     # the header promises that the allocation-free decode entry's fixed
     # scratch array serves every M <= 16 under the current split-K plan

@@ -192,12 +192,32 @@ def test_gemm_split_k_is_deterministic_and_matches():
     assert_close(to_f64(Y1)[np.ix_(rows, cols)], Y_ref, A, "split-K 5120x5120 M=256")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,K,N", [(17, 1024, 150 * 128), (40, 2048, 150 * 128 + 72)])
+def test_gemm_whole_waves_and_split_tail_all_outputs(dtype, M, K, N):
+    # 150 output tiles of 128 columns: one full wave of 148 whole tiles, and
+    # the 2 tiles left over cut along K (the split-tail schedule), every
+    # output checked, run twice for determinism
+    assert w4.workspace_bytes(M, N, K) > 0  # the leftover tiles need partial tiles
+    W = gaussian_weights(K, N, 0.02, M + N)
+    dev_t, _ = _int4_dev(W)
+    X = activations(M, K, dtype, M).cuda()
+    st = _status()
+    Y1 = w4.gemm(X, *dev_t[:3], dev_status=st)
+    Y2 = w4.gemm(X, *dev_t[:3], dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    Y_ref, A = int4_expected(W, X.cpu().double().numpy(), dtype)
+    assert_close(to_f64(Y1), Y_ref, A, f"split tail M={M} K={K} N={N} {dtype}")
+
+
 def test_tickets_are_left_at_zero():
     # the split-K tickets wrap back to zero at each block's contributor count:
     # after decode calls (split column blocks on every shape below) and a
     # split-K prefill call through one workspace, the ticket area is all zero
     ticket_bytes = 4096 * 8 * 4  # one int per 32-column slice of up to 4096 column blocks
-    shapes = [(1, 5120, 5120), (5, 27648, 1024), (16, 2048, 3072), (256, 5120, 1280)]
+    shapes = [(1, 5120, 5120), (5, 27648, 1024), (16, 2048, 3072), (256, 5120, 1280), (17, 1024, 150 * 128)]
     need = max(w4.workspace_bytes(M, N, K) for M, K, N in shapes)
     ws = torch.zeros(need, dtype=torch.uint8, device=dev())
     st = _status()
