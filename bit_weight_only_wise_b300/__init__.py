@@ -56,6 +56,7 @@ _SIGS = {
     "nf4_double_quantize": [_vp, _i, _i, _i, _vp, _vp, _vp],
     "w4a16_repack_awq": [_vp, _vp, _i, _i, _i, _vp, _vp, _vp],
     "w4a16_gemm_silu_mul": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp],
+    "w4a16_gemv_batch": [_vp, _i, _vp, _sz, _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -164,6 +165,60 @@ def gemm(X, qweight, scales, qzeros, g_idx=None, out=None, group_size=GROUP_SIZE
 def gemv(X, qweight, scales, qzeros, g_idx=None, out=None, group_size=GROUP_SIZE, ws=None, dev_status=None):
     """Y = X . W_hat (INT4), M <= 16 (the split-K decode kernel)."""
     return _int4_call("w4a16_gemv", X, qweight, scales, qzeros, g_idx, out, group_size, ws, dev_status)
+
+
+class _GemvItem(ctypes.Structure):
+    """The C struct w4a16_gemv_item."""
+    _fields_ = [("X", _vp), ("qweight", _vp), ("scales", _vp), ("qzeros", _vp), ("g_idx", _vp), ("Y", _vp),
+                ("M", _i), ("N", _i), ("K", _i), ("group_size", _i), ("dtype", _i)]
+
+
+class GemvBatch:
+    """A fixed list of decode products (each as ``gemv`` would compute it),
+    launched in order by one library call (``w4a16_gemv_batch``) each time the
+    object is called.
+
+    ``items``: a sequence of ``(X, qweight, scales, qzeros, Y)`` tuples, or
+    of dicts with those keys plus optional ``g_idx`` and ``group_size``.  The
+    tensors are checked once, here, and kept alive by the object; a call
+    re-reads their current contents (so X can be refilled between calls).
+    """
+
+    def __init__(self, items, ws=None, dev_status=None):
+        rows, self._keep = [], []
+        need, device = 0, None
+        for it in items:
+            d = dict(zip(("X", "qweight", "scales", "qzeros", "Y"), it)) if not isinstance(it, dict) else dict(it)
+            X, qw, Y = d["X"], d["qweight"], d["Y"]
+            K, N = qw.shape[0] * 8, qw.shape[1]
+            _check_x(X, K)
+            M = X.shape[0]
+            _out(X, N, Y)
+            g = d.get("group_size", GROUP_SIZE)
+            rows.append(_GemvItem(_ptr(X), _ptr(qw), _ptr(d["scales"]), _ptr(d.get("qzeros")), _ptr(d.get("g_idx")),
+                                  _ptr(Y), M, N, K, g, _DTYPES[X.dtype]))
+            self._keep.append(d)
+            need = max(need, workspace_bytes(M, N, K))
+            device = X.device
+        self._items = (_GemvItem * max(1, len(rows)))(*rows)
+        self._count = len(rows)
+        if ws is None and need and device is not None:
+            ws = workspace(1, 1, 1, device, nbytes=need)
+        self._ws = ws
+        self._ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+        self._status = dev_status
+        self._device = device
+
+    def __call__(self):
+        if self._count:
+            st = _lib.w4a16_gemv_batch(ctypes.addressof(self._items), self._count, _ptr(self._ws), self._ws_bytes,
+                                       _ptr(self._status), _stream(self._device))
+            _check(st, "w4a16_gemv_batch")
+
+
+def gemv_batch(items, ws=None, dev_status=None):
+    """Run a list of decode products once (see ``GemvBatch``)."""
+    GemvBatch(items, ws, dev_status)()
 
 
 def gemm_silu_mul(X, qweight, scales, qzeros, out=None, group_size=GROUP_SIZE, ws=None, dev_status=None):

@@ -112,6 +112,23 @@ w4a16_status check_int4_ptrs(const void* X, const uint32_t* qweight, const void*
   return W4A16_OK;
 }
 
+// w4a16_gemv's checks before anything launches; *empty: a valid call with
+// nothing to compute (M or N zero)
+w4a16_status gemv_check(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                        const int32_t* g_idx, const void* Y, int M, int N, int K, int group_size,
+                        w4a16_dtype dtype, bool* empty) {
+  *empty = false;
+  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
+  w4a16_status st = check_int4_shape(M, N, K, group_size);
+  if (st != W4A16_OK) return st;
+  if (M > W4A16_GEMV_MAX_M) return W4A16_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    *empty = true;
+    return W4A16_OK;
+  }
+  return check_int4_ptrs(X, qweight, scales, qzeros, g_idx, Y);
+}
+
 }  // namespace
 
 extern "C" {
@@ -119,15 +136,35 @@ extern "C" {
 w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
                         const int32_t* g_idx, void* Y, int M, int N, int K, int group_size, w4a16_dtype dtype,
                         void* workspace, size_t workspace_bytes, int* dev_status, cudaStream_t stream) {
-  if (!ok_dtype(dtype)) return W4A16_ERR_INVALID_ARG;
-  w4a16_status st = check_int4_shape(M, N, K, group_size);
-  if (st != W4A16_OK) return st;
-  if (M > W4A16_GEMV_MAX_M) return W4A16_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return W4A16_OK;
-  st = check_int4_ptrs(X, qweight, scales, qzeros, g_idx, Y);
-  if (st != W4A16_OK) return st;
+  bool empty = false;
+  const w4a16_status st = gemv_check(X, qweight, scales, qzeros, g_idx, Y, M, N, K, group_size, dtype, &empty);
+  if (st != W4A16_OK || empty) return st;
   return int4_gemv_impl(X, qweight, scales, qzeros, g_idx, Y, M, N, K, group_size, dtype, workspace,
                         workspace_bytes, dev_status, stream);
+}
+
+w4a16_status w4a16_gemv_batch(const w4a16_gemv_item* items, int count, void* workspace, size_t workspace_bytes,
+                              int* dev_status, cudaStream_t stream) {
+  if (count < 0 || (count > 0 && items == nullptr)) return W4A16_ERR_INVALID_ARG;
+  // every item is checked before the first launch
+  for (int i = 0; i < count; ++i) {
+    const w4a16_gemv_item& it = items[i];
+    bool empty = false;
+    w4a16_status st = gemv_check(it.X, it.qweight, it.scales, it.qzeros, it.g_idx, it.Y, it.M, it.N, it.K,
+                                 it.group_size, it.dtype, &empty);
+    if (st != W4A16_OK) return st;
+    if (empty) continue;
+    st = check_workspace(gemv_plan(it.M, it.N, it.K, it.g_idx ? kInt4Act : kInt4), workspace, workspace_bytes);
+    if (st != W4A16_OK) return st;
+  }
+  for (int i = 0; i < count; ++i) {
+    const w4a16_gemv_item& it = items[i];
+    if (it.M == 0 || it.N == 0) continue;
+    const w4a16_status st = int4_gemv_impl(it.X, it.qweight, it.scales, it.qzeros, it.g_idx, it.Y, it.M, it.N, it.K,
+                                           it.group_size, it.dtype, workspace, workspace_bytes, dev_status, stream);
+    if (st != W4A16_OK) return st;
+  }
+  return W4A16_OK;
 }
 
 w4a16_status w4a16_gemm(const void* X, const uint32_t* qweight, const void* scales, const uint32_t* qzeros,

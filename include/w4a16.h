@@ -148,6 +148,34 @@ w4a16_status w4a16_gemv(const void* X, const uint32_t* qweight, const void* scal
                         cudaStream_t stream);
 
 /*
+ * A list of decode products launched by one call: items[i] holds the
+ * arguments of one w4a16_gemv call (same meaning, layouts and limits), and
+ * the products run in the order given on `stream`, each computing exactly
+ * what w4a16_gemv computes for its item.  They use `workspace` in turn, so
+ * it must hold at least the largest w4a16_workspace_bytes(M, N, K) of the
+ * items.  The call spares a caller that runs many small products per step
+ * (a decoder's linears for one token) a library call per product.
+ *   items: host memory, read during the call only (count 0: nothing to do).
+ *   Errors: every item is checked before anything is launched; an invalid
+ *   item returns its status (W4A16_ERR_INVALID_ARG or _UNSUPPORTED) with
+ *   nothing launched.  A launch error returns W4A16_ERR_CUDA after the items
+ *   before it were launched.
+ */
+typedef struct w4a16_gemv_item {
+  const void* X;
+  const uint32_t* qweight;
+  const void* scales;
+  const uint32_t* qzeros; /* NULL: symmetric */
+  const int32_t* g_idx;   /* NULL: groups in order */
+  void* Y;
+  int M, N, K, group_size;
+  w4a16_dtype dtype;
+} w4a16_gemv_item;
+
+w4a16_status w4a16_gemv_batch(const w4a16_gemv_item* items, int count, void* workspace, size_t workspace_bytes,
+                              int* dev_status, cudaStream_t stream);
+
+/*
  * Fused decoder-MLP activation: A[M, F] = SiLU(X . W_hat[:, :F]) * (X . W_hat[:, F:])
  * for a gate_up weight of N = 2F columns (gate in columns [0, F), up in
  * [F, 2F)), SiLU(t) = t / (1 + e^-t), both products and the activation in

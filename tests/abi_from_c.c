@@ -9,6 +9,7 @@
 #include <limits.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stddef.h>
 #include <string.h>
 
 #include "w4a16.h"
@@ -61,6 +62,10 @@ static int fuzz_sizes(void) {
             s1 = w4a16_gemv(NULL, PU(16), P(16), PU(16), NULL, P(16), M, N, K, G, dt, NULL, 0, NULL, NULL);
             s2 = w4a16_gemv_noalloc(NULL, PU(16), P(16), PU(16), NULL, P(16), M, N, K, G, dt, NULL, NULL);
             CHECK(defined_host_status(s1) && s1 == s2);
+            {  /* a one-item batch answers as w4a16_gemv */
+              const w4a16_gemv_item it = {NULL, PU(16), P(16), PU(16), NULL, P(16), M, N, K, G, dt};
+              CHECK(w4a16_gemv_batch(&it, 1, NULL, 0, NULL, NULL) == s1);
+            }
             CHECK(defined_host_status(w4a16_gemm_prepacked(NULL, PU(16), P(16), PU(16), PI(16), P(16), M, N, K, G,
                                                            dt, P(16), 1u << 20, NULL, NULL)));
             CHECK(defined_host_status(
@@ -100,6 +105,7 @@ int main(void) {
       (fn_t)nf4_default_codebook, (fn_t)nf4dq_gemm,
       (fn_t)nf4dq_dequant,       (fn_t)nf4_double_quantize,
       (fn_t)w4a16_repack_awq,    (fn_t)w4a16_gemm_silu_mul,
+      (fn_t)w4a16_gemv_batch,
   };
   for (size_t i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i) CHECK(fns[i] != NULL);
 
@@ -138,6 +144,22 @@ int main(void) {
   CHECK(nf4_gemm(P(16), PU(16), PF(16), PF(16), P(16), 4, 64, 256, 32, W4A16_BF16, NULL, 0, NULL, NULL) ==
         W4A16_ERR_UNSUPPORTED);
   CHECK(w4a16_selftest_wait_timeout(NULL, 1000, NULL) == W4A16_ERR_INVALID_ARG);
+
+  /* the batch entry: its item layout (the Python binding mirrors it), the
+   * empty batch, and an invalid item anywhere in the list rejected before
+   * any launch */
+  CHECK(sizeof(w4a16_gemv_item) == 72 && offsetof(w4a16_gemv_item, M) == 48 &&
+        offsetof(w4a16_gemv_item, dtype) == 64);
+  CHECK(w4a16_gemv_batch(NULL, 0, NULL, 0, NULL, NULL) == W4A16_OK);
+  CHECK(w4a16_gemv_batch(NULL, -1, NULL, 0, NULL, NULL) == W4A16_ERR_INVALID_ARG);
+  CHECK(w4a16_gemv_batch(NULL, 1, NULL, 0, NULL, NULL) == W4A16_ERR_INVALID_ARG);
+  {
+    const w4a16_gemv_item two[2] = {
+        {P(16), PU(16), P(16), PU(16), NULL, P(16), 1, 64, 256, 128, W4A16_BF16},   /* valid */
+        {P(16), PU(16), P(16), PU(16), NULL, P(16), 17, 64, 256, 128, W4A16_BF16},  /* M > 16 */
+    };
+    CHECK(w4a16_gemv_batch(two, 2, NULL, 0, NULL, NULL) == W4A16_ERR_INVALID_ARG);
+  }
 
   /* size limits */
   CHECK(w4a16_gemm(P(16), PU(16), P(16), PU(16), NULL, P(16), W4A16_MAX_M + 1, 64, 256, 128, W4A16_BF16, NULL, 0,

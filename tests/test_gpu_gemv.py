@@ -81,6 +81,39 @@ def test_gemv_deterministic_and_workspace_reuse():
     assert torch.equal(Y3.view(torch.int16), Y5.view(torch.int16))
 
 
+def test_gemv_batch_equals_single_calls():
+    # one w4a16_gemv_batch call over mixed items (dtypes, M, act-order,
+    # symmetric groups of 64, an empty item) computes each product exactly as
+    # its own w4a16_gemv call does, through one shared workspace, twice
+    items, singles = [], []
+    cases = [(1, 1024, 776, "bf16", False, 128, False), (5, 2048, 512, "f16", False, 128, False),
+             (16, 1536, 264, "bf16", True, 128, False), (3, 1024, 520, "f16", False, 64, True),
+             (0, 512, 256, "bf16", False, 128, False)]
+    for i, (M, K, N, dtype, act, g, sym) in enumerate(cases):
+        W = gaussian_weights(K, N, 0.02, 50 + i)
+        g_idx = act_order_g_idx(K, g, i) if act else None
+        if sym:
+            q, sc = int4.rtn_quantize_sym(W, g)
+            qw, qz = to_dev_u32(int4.pack_along_k(q)), None
+        else:
+            qwp, scp, qzp, _, _ = int4.quantize_packed(W, g, g_idx)
+            qw, sc, qz = to_dev_u32(qwp), scp, to_dev_u32(qzp)
+        gi = None if g_idx is None else to_dev(g_idx)
+        X = activations(max(M, 1), K, dtype, i).cuda()[:M].contiguous()
+        Y = torch.full((M, N), 7.0, dtype=TDT[dtype], device="cuda")
+        items.append(dict(X=X, qweight=qw, scales=to_dev(sc), qzeros=qz, Y=Y, g_idx=gi, group_size=g))
+        singles.append(w4.gemv(X, qw, to_dev(sc), qz, g_idx=gi, group_size=g) if M else None)
+    batch = w4.GemvBatch(items)
+    for _ in range(2):
+        for it in items:
+            it["Y"].fill_(7.0)
+        batch()
+        torch.cuda.synchronize()
+        for it, Y1 in zip(items, singles):
+            if Y1 is not None:
+                assert torch.equal(it["Y"].view(torch.int16), Y1.view(torch.int16))
+
+
 def test_gemm_entry_dispatches_small_m_to_gemv():
     K, N = 1024, 512
     W = gaussian_weights(K, N, 0.02, 1)
