@@ -16,17 +16,18 @@
 //   producer warp  streams each unit (256 columns x 128 rows along K) into a
 //                  shared-memory stage: eight 2-KB weight boxes (16 word-rows
 //                  x 32 columns, 128-byte swizzle) and the activation box by
-//                  TMA, and the unit's metadata (grouped INT4: the scales and
-//                  zero words of its 1, 2 or 4 groups by cp.async; NF4: the
-//                  absmax of its two 64-row blocks by TMA, or their 8-bit
-//                  codes and second-level scales by cp.async; act-order: the
-//                  128 rows' group indices by cp.async), all completing on the
-//                  stage's `full` barrier;
-//   helper warp    turns the raw metadata into what the consumers read (packed
-//                  per-column dequantization constants; fp32 absmax; table
-//                  offsets), and the raw activations into the MMA B-operand
-//                  pairs, once per stage for all consumers, then arrives on
-//                  `ready`;
+//                  TMA, and the unit's metadata (NF4: the absmax of its two
+//                  64-row blocks by TMA, or their 8-bit codes and
+//                  second-level scales by cp.async; act-order: the 128 rows'
+//                  group indices by cp.async), all completing on the stage's
+//                  `full` barrier;
+//   helper warp    copies grouped INT4 metadata (the scales and zero words of
+//                  a unit's 1, 2 or 4 groups, by cp.async onto the same
+//                  barrier, S units ahead), turns the raw metadata into what
+//                  the consumers read (packed per-column dequantization
+//                  constants; fp32 absmax; table offsets), and the raw
+//                  activations into the MMA B-operand pairs, once per stage
+//                  for all consumers, then arrives on `ready`;
 //   8 consumer     each own a 32-column slice of the unit: four 16-byte
 //   warps          weight loads, the activation pairs and the constants from
 //                  shared memory, exact dequantization in registers and
@@ -46,8 +47,8 @@
 // gemv_common.cuh.
 //
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag and
-// the caller's status word, and the producer lets its copies in flight land
-// before the CTA exits.
+// the caller's status word, and the producer and helper let their copies in
+// flight land before the CTA exits.
 #include <cuda.h>
 
 #include "dq_common.cuh"
@@ -223,6 +224,40 @@ __device__ __forceinline__ uint32_t dq_pair_rows(uint32_t code, uint32_t zm, uin
   return pack2_rn(lo, hi, BF16);
 }
 
+// INT4: unit u's scales and zero words into the raw area of a side stage
+// (side: its shared address), one cp.async arrival on `bar` per lane.  The
+// helper warp issues these, S units ahead of the unit it converts: the
+// producer warp is on the critical path (every instruction it spends per unit
+// shows in the kernel's time) and the helper has time to spare; moving them
+// measured 1-6% faster across the decode shapes.  Symmetric weights: a.nwz =
+// 0, so the zero words are zero-filled (the helper turns them into 8s).
+template <int NT, int FMT, int GPU, bool SILU>
+__device__ __forceinline__ void int4_meta_copy(const GemvArgs& a, uint32_t side, const UnitWalk<GPU>& u, int lane,
+                                               uint64_t* bar) {
+  using L = WsLayout<NT, FMT, GPU>;
+  using G = Geom<SILU>;
+  const int cpb = G::cpb(a);
+  const int scol_l = 8 * (lane & 15) + (lane >> 4) * G::hiofs(a);
+  const int ocol_l = 8 * (lane & 15) + (lane >> 4) * G::hi2(a);
+  const int zw_l = (lane >> 4) * (G::hiofs(a) >> 3) + (lane & 15);
+  const int nw = a.N >> 3;
+  const int b = u.b;
+#pragma unroll
+  for (int j = 0; j < L::NGRP; ++j) {
+    const int gi = u.group(j);
+    const bool gv = GPU <= 1 || gi < a.NG;  // only 32/64-row groups can run past K
+    const int col = b * cpb + scol_l;
+    const bool sv = gv && b * cpb + ocol_l < G::nout(a);
+    cp_async_16(side + L::RAW + j * (kGemvCols * 2) + 16 * lane, sv ? a.scales + (size_t)gi * a.N + col : a.scales,
+                sv);
+    const int zc = b * (cpb >> 3) + zw_l;
+    const bool zv = sv && zc < a.nwz;
+    cp_async_4(side + L::RAW + L::NGRP * (kGemvCols * 2) + j * 128 + 4 * lane, zv ? a.qz + (size_t)gi * nw + zc : a.qw,
+               zv);
+  }
+  cp_async_arrive_noinc(bar);
+}
+
 // ------------------------------------------------------------------ roles
 template <int NT, int FMT, int GPU, bool SILU>
 __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmA,
@@ -248,27 +283,13 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   const int scol_l = 8 * (lane & 15) + (lane >> 4) * G::hiofs(a);
   const int ocol_l = 8 * (lane & 15) + (lane >> 4) * G::hi2(a);
   const int zw_l = (lane >> 4) * (G::hiofs(a) >> 3) + (lane & 15);
-  // the unit's metadata into stage s, by cp.async (NF4's absmax by TMA)
+  // the unit's metadata into stage s: by cp.async (NF4's absmax by TMA;
+  // INT4's scales and zeros by the helper warp)
   auto issue_meta = [&](int s, const UnitWalk<GPU>& u) {
     const uint32_t side = side0 + s * L::SIDE;
     const int b = u.b, kb = u.kb;
     if constexpr (FMT == kInt4) {
-#pragma unroll
-      for (int j = 0; j < L::NGRP; ++j) {
-        const int gi = u.group(j);
-        const bool gv = GPU <= 1 || gi < a.NG;  // only 32/64-row groups can run past K
-        const int col = b * cpb + scol_l;
-        const bool sv = gv && b * cpb + ocol_l < G::nout(a);
-        cp_async_16(side + L::RAW + j * (kGemvCols * 2) + 16 * lane, sv ? a.scales + (size_t)gi * a.N + col : a.scales,
-                    sv);
-        // symmetric weights: a.nwz = 0, so the zero words are zero-filled
-        // (the helper turns them into 8s)
-        const int zc = b * (cpb >> 3) + zw_l;
-        const bool zv = sv && zc < a.nwz;
-        cp_async_4(side + L::RAW + L::NGRP * (kGemvCols * 2) + j * 128 + 4 * lane,
-                   zv ? a.qz + (size_t)gi * nw + zc : a.qw, zv);
-      }
-      cp_async_arrive_noinc(&full[s]);
+      // INT4 metadata: copied by the helper warp (int4_meta_copy)
     } else if constexpr (FMT == kNF4) {
       if (lane == kCW) tma_load_2d(smem + S * kWBytes + s * L::SIDE + L::CT, tmA, &full[s], b * kGemvCols, kb * 2);
     } else if constexpr (FMT == kNF4DQ) {
@@ -357,16 +378,31 @@ __device__ __forceinline__ void ws_producer(const CUtensorMap* tmW, const CUtens
   cp_async_wait_all();
 }
 
-template <int NT, int FMT, bool BF16, int GPU>
+template <int NT, int FMT, bool BF16, int GPU, bool SILU>
 __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint64_t* full, uint64_t* ready,
-                                          volatile int* abort, int nu, int lane) {
+                                          volatile int* abort, int nu, int b0, int k0, int lane) {
   using L = WsLayout<NT, FMT, GPU>;
   const int S = stages_of<NT, FMT, GPU>(a);
   const int gl = lane >> 2, c = lane & 3;
+  const uint32_t side0 = smem_u32(smem) + S * kWBytes;
+  // INT4: this warp copies each unit's metadata, S units ahead: a stage's raw
+  // area is free once this warp has converted it
+  UnitWalk<GPU> um(a, b0, k0);
+  if constexpr (FMT == kInt4) {
+    griddep_wait();  // the scales and zeros may be written by the previous kernel
+    const int n_first = nu < S ? nu : S;
+    for (int k = 0; k < n_first; ++k) {
+      int4_meta_copy<NT, FMT, GPU, SILU>(a, side0 + k * L::SIDE, um, lane, &full[k]);
+      um.next(a);
+    }
+  }
   int s = 0;
   uint32_t ph = 0;
   for (int k = 0; k < nu; ++k) {
-    if (!mbar_wait(&full[s], ph, abort, a.dev_status, kWaitLimitNs)) return;
+    if (!mbar_wait(&full[s], ph, abort, a.dev_status, kWaitLimitNs)) {
+      cp_async_wait_all();
+      return;
+    }
     uint8_t* st = smem + S * kWBytes + s * L::SIDE;
     if constexpr (FMT == kInt4) {
       // constants of columns 8*lane .. 8*lane+7 of the unit: consumer warp
@@ -409,6 +445,10 @@ __device__ __forceinline__ void ws_helper(const GemvArgs& a, uint8_t* smem, uint
         ct[9] = make_uint4(k1[4], k1[5], k1[6], k1[7]);
         ct[16] = make_uint4(k2[0], k2[1], k2[2], k2[3]);
         ct[17] = make_uint4(k2[4], k2[5], k2[6], k2[7]);
+      }
+      if (k + S < nu) {
+        int4_meta_copy<NT, FMT, GPU, SILU>(a, side0 + s * L::SIDE, um, lane, &full[s]);
+        um.next(a);
       }
     } else if constexpr (FMT == kNF4DQ) {
       // absmax_hat = fl32(code * s2) for [2 blocks][256 columns]: lane takes
@@ -767,7 +807,7 @@ __global__ void __launch_bounds__(kWsThreads, FMT == kInt4Act ? 1 : 2)
   if (warp == kProducer)
     ws_producer<NT, FMT, GPU, SILU>(&tmW, &tmX, &tmA, a, smem, full, empty, abort, nu, b0, k0, lane);
   else if (warp == kHelper)
-    ws_helper<NT, FMT, BF16, GPU>(a, smem, full, ready, abort, nu, lane);
+    ws_helper<NT, FMT, BF16, GPU, SILU>(a, smem, full, ready, abort, nu, b0, k0, lane);
   else
     ws_consumer<NT, FMT, BF16, GPU, SILU>(a, R, smem, s_cb, ready, empty, abort, nu, b0, k0, warp, lane);
 }
