@@ -16,13 +16,13 @@
 //   warp 1     allocates TMEM; one lane issues the MMAs (4 x K=16 per stage)
 //              and commits them to mbarriers that free the stage and the A
 //              buffer.
-//   warps 2-17 dequantize, in two groups of 8 that take alternate K blocks
-//              (so two blocks' loads, arithmetic and TMEM stores overlap):
-//              thread = one output column (its TMEM lane), each of the two
-//              warps of a group sharing a lane quarter takes 4 of the stage's
-//              8 word-rows; codes -> exact fp16/bf16 pairs in natural K order
-//              -> tcgen05.st into one of 4 A buffers.  After the K loop the
-//              16 warps read D back (tcgen05.ld) and write Y.
+//   warps 2-17 dequantize, in four groups of 4 that take the K blocks in
+//              turn (so four blocks' loads, arithmetic and TMEM stores
+//              overlap): thread = one output column (its TMEM lane), all 8
+//              word-rows (64 K rows) of the stage; codes -> exact fp16/bf16
+//              pairs in natural K order -> tcgen05.st into one of 4 A
+//              buffers.  After the K loop the 16 warps read D back
+//              (tcgen05.ld) and write Y.
 //
 // Dequantization follows the pages' format (cloud.tencent.com/developer/
 // article/2726413 §2.1-2.2: asymmetric, one scale and zero point per group of
@@ -52,14 +52,14 @@ constexpr int kStages = 4;
 constexpr int kABufs = 4;
 constexpr int kDqWarps = 16;                      // dequantizing warps
 constexpr int kParts = kDqWarps / 4;              // warps sharing one TMEM lane quarter
-// The dequantizing warps form two groups that take alternate K blocks, so two
-// blocks are in flight: one group's loads, arithmetic and TMEM stores overlap
-// the other's.
-constexpr int kDqGroups = 2;
+// The dequantizing warps form four groups (one warp per TMEM lane quarter
+// each) that take the K blocks in turn, so four blocks are in flight: one
+// group's loads, arithmetic and TMEM stores overlap the others'.
+constexpr int kDqGroups = 4;
 constexpr int kGroupWarps = kDqWarps / kDqGroups;
 constexpr int kWords = (kBK / 8) / (kGroupWarps / 4);  // packed words per thread per stage
-static_assert(kWords == 4 && kStages % kDqGroups == 0 && kABufs % kDqGroups == 0,
-              "each group keeps to its own stages and A buffers");
+static_assert(kGroupWarps == 4 && kWords == 8 && kStages % kDqGroups == 0 && kABufs % kDqGroups == 0,
+              "each group keeps to its own stages and A buffers; a thread takes a whole stage");
 constexpr int kThreads = 32 * (2 + kDqWarps);
 constexpr int kWStageBytes = (kBK / 8) * kBN * 4;  // 4 KB
 constexpr uint32_t kTmemCols = 512;
@@ -79,7 +79,9 @@ struct __align__(8) Bars {
   float cb[16];
 };
 
-enum { kFmtInt4 = 0, kFmtInt4Act = 1, kFmtNF4 = 2 };
+// kFmtInt4G32: INT4 with groups of 32 rows, so a 64-row K block's two halves
+// have their own scales and zero points
+enum { kFmtInt4 = 0, kFmtInt4Act = 1, kFmtNF4 = 2, kFmtInt4G32 = 3 };
 
 // Act-order keeps every group's (scale, zero) of the CTA's 128 columns in
 // shared memory, so its token tile is capped at 128 to leave room.
@@ -248,8 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- dequant + epilogue
     const int dw = warp - 2;
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
-    const int grp = dw / kGroupWarps;          // K blocks grp, grp + 2, ...
-    const int h = (dw % kGroupWarps) >> 2;     // which kWords word-rows of a stage
+    const int grp = dw / kGroupWarps;          // K blocks grp, grp + 4, ...
     const int ep = dw >> 2;                    // epilogue: which quarter of the tokens
     const int nl = quarter * 32 + lane;
     const int n = w0 + (nl >> 6) * p.hiofs + (nl & 63);     // weight column
@@ -258,39 +259,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
     // the current K block's constants, with the raw values of this group's
-    // next two blocks in flight, so a global load has four blocks' worth of
-    // MMAs to land
+    // next two blocks in flight, so a global load has many blocks' worth of
+    // MMAs to land.  Groups of 32 rows: s_* holds the two halves' fp16 scales
+    // (low: rows 0-31, high: rows 32-63), z_* their zero points (bits 0-7,
+    // 8-15).
+    constexpr bool kInt4 = FMT == kFmtInt4 || FMT == kFmtInt4G32;
+    constexpr bool kTwo = FMT == kFmtInt4G32;
     uint32_t s_raw = 0, z_raw = 0, s_nxt = 0, z_nxt = 0, s_nx2 = 0, z_nx2 = 0;
     float am = 0.f, am_nxt = 0.f, am_nx2 = 0.f;
+    auto group_sz = [&](int g, uint32_t& s_out, uint32_t& z_out) {
+      if (g >= p.NG) {  // rows past K (a last block shorter than 64 rows): X is zero there
+        s_out = z_out = 0;
+        return;
+      }
+      s_out = p.scales[(size_t)g * p.N + n];
+      z_out = p.qz ? (p.qz[(size_t)g * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu : 8u;
+    };
     auto fetch = [&](int kb, uint32_t& s_out, uint32_t& z_out, float& am_out) {  // kb: absolute K block
       if (!ok || kb >= kb0 + nkb || FMT == kFmtInt4Act) return;
-      if (FMT == kFmtInt4) {
-        // this thread's 32 rows of the 64-row block lie in one group (groups
-        // of 32, 64, any multiple of 128, or one group for all of K): the
-        // group of 32-row chunk 2 kb + h is floor(chunk / (g / 32)), taken as
-        // a multiply-high by the host's gmagic = ceil(2^31 / (g / 32)), exact
-        // for every chunk index below 2^14 and divisor up to 2^14
-        const int grp = (int)__umulhi((uint32_t)(2 * (2 * kb + h)), p.gmagic);
-        if (grp >= p.NG) {  // rows past K (a last block shorter than 64 rows): X is zero there
-          s_out = z_out = 0;
-          return;
-        }
-        s_out = p.scales[(size_t)grp * p.N + n];
-        z_out = p.qz ? (p.qz[(size_t)grp * (p.N >> 3) + (n >> 3)] >> (4 * (n & 7))) & 0xFu : 8u;
+      if (kTwo) {
+        uint32_t s1, z1;
+        group_sz(2 * kb, s_out, z_out);
+        group_sz(2 * kb + 1, s1, z1);
+        s_out |= s1 << 16;
+        z_out |= z1 << 8;
+      } else if (kInt4) {
+        // the block lies in one group (groups of 64, any multiple of 128
+        // rows, or one group for all of K): the group of 32-row chunk 2 kb is
+        // floor(2 kb / (g / 32)), taken as a multiply-high by the host's
+        // gmagic = ceil(2^31 / (g / 32)), exact for every chunk index below
+        // 2^14 and divisor up to 2^14
+        group_sz((int)__umulhi((uint32_t)(4 * kb), p.gmagic), s_out, z_out);
       } else if (p.absmax_q) {  // double quantization: absmax_hat = fl32(code * s2)
         am_out = __fmul_rn((float)p.absmax_q[(size_t)kb * p.N + n], p.absmax_s2[(size_t)kb * p.nc2 + (n >> 8)]);
       } else {
         am_out = p.absmax[(size_t)kb * p.N + n];  // 64-row blocks == stages
       }
     };
-    // this group's K blocks are kb0 + grp + 2i: one 128-row INT4 group (kb0 is
-    // group aligned), or one 64-row NF4 block, apart
+    // this group's K blocks are kb0 + grp + 4i
     constexpr int kStep = kDqGroups;
     fetch(kb0 + grp, s_raw, z_raw, am);
     fetch(kb0 + grp + kStep, s_nxt, z_nxt, am_nxt);
     fetch(kb0 + grp + 2 * kStep, s_nx2, z_nx2, am_nx2);
-    uint32_t zmix = dq_zmix_f16(z_raw), s2 = s_raw * 0x10001u;
-    DqConstBF16Fma cbf = dq_const_bf16_fma(z_raw, s_raw);
+    // constants of rows 0-31 (…0) and 32-63 (…1) of the block
+    uint32_t zmix0 = 0, s20 = 0, zmix1 = 0, s21 = 0;
+    DqConstBF16Fma cbf0{}, cbf1{};
+    auto make_consts = [&]() {
+      if (!kInt4) return;
+      const uint32_t z0 = kTwo ? z_raw & 0xFFu : z_raw, s0 = kTwo ? s_raw & 0xFFFFu : s_raw;
+      if (BF16) {
+        cbf0 = dq_const_bf16_fma(z0, s0);
+        cbf1 = kTwo ? dq_const_bf16_fma(z_raw >> 8, s_raw >> 16) : cbf0;
+      } else {
+        zmix0 = dq_zmix_f16(z0);
+        s20 = s0 * 0x10001u;
+        zmix1 = kTwo ? dq_zmix_f16(z_raw >> 8) : zmix0;
+        s21 = kTwo ? (s_raw >> 16) * 0x10001u : s20;
+      }
+    };
+    make_consts();
 
     bool alive = true;
     for (int it = grp; it < nkb && alive; it += kDqGroups) {
@@ -304,13 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         z_nxt = z_nx2;
         am_nxt = am_nx2;
         fetch(kb0 + it + 2 * kStep, s_nx2, z_nx2, am_nx2);
-        if (FMT == kFmtInt4) {
-          if (BF16) cbf = dq_const_bf16_fma(z_raw, s_raw);
-          else {
-            zmix = dq_zmix_f16(z_raw);
-            s2 = s_raw * 0x10001u;
-          }
-        }
+        make_consts();
       }
       if (!mbar_wait(&bars->full[s], (it / kStages) & 1, abort, p.dev_status, kWaitLimitNs)) {
         alive = false;
@@ -319,13 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t wv[kWords];
       const uint32_t* wst = sw + s * (kWStageBytes / 4);
 #pragma unroll
-      for (int i = 0; i < kWords; ++i) wv[i] = wst[(nl >> 6) * (kBN / 2) * (kBK / 8) + (kWords * h + i) * (kBN / 2) + (nl & 63)];
+      for (int i = 0; i < kWords; ++i) wv[i] = wst[(nl >> 6) * (kBN / 2) * (kBK / 8) + i * (kBN / 2) + (nl & 63)];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->empty[s]);
       uint32_t regs[4 * kWords];
       if constexpr (FMT == kFmtInt4Act) {
-        // every K row has its own group: rows 64*it + 8*(kWords*h + i) + 2j, +1
-        const int4* gp = reinterpret_cast<const int4*>(p.g_idx + (kb0 + it) * kBK + 8 * kWords * h);
+        // every K row has its own group: rows 64*it + 8*i + 2j, +1
+        const int4* gp = reinterpret_cast<const int4*>(p.g_idx + (kb0 + it) * kBK);
 #pragma unroll
         for (int i = 0; i < kWords; ++i) {
           const int4 ga = __ldg(gp + 2 * i), gb = __ldg(gp + 2 * i + 1);
@@ -355,15 +376,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kWords; ++i) {
           uint32_t* o = regs + 4 * i;
           if (FMT == kFmtNF4) dq_word_nat_nf4<BF16>(wv[i], bars->cb, am, o);
-          else if (BF16) dq_word_nat_bf16_fma(wv[i], cbf, o);
-          else dq_word_nat_f16(wv[i], zmix, s2, o);
+          else if (BF16) dq_word_nat_bf16_fma(wv[i], i < kWords / 2 ? cbf0 : cbf1, o);
+          else dq_word_nat_f16(wv[i], i < kWords / 2 ? zmix0 : zmix1, i < kWords / 2 ? s20 : s21, o);
         }
       }
       if (!mbar_wait(&bars->a_empty[b], ((it / kABufs) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) {
         alive = false;
         break;
       }
-      tmem_st_x16(tmem + lane_off + kTmemA + 32u * b + 16u * h, regs);
+      tmem_st_x16(tmem + lane_off + kTmemA + 32u * b, regs);
+      tmem_st_x16(tmem + lane_off + kTmemA + 32u * b + 16u, regs + 16);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -615,6 +637,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool bf16, bool nf4, cudaStream_t 
   if (act)
     return bf16 ? launch_tc<kFmtInt4Act, true>(tmX, tmW, p, grid, st)
                 : launch_tc<kFmtInt4Act, false>(tmX, tmW, p, grid, st);
+  if (a.gsize == 32)
+    return bf16 ? launch_tc<kFmtInt4G32, true>(tmX, tmW, p, grid, st)
+                : launch_tc<kFmtInt4G32, false>(tmX, tmW, p, grid, st);
   return bf16 ? launch_tc<kFmtInt4, true>(tmX, tmW, p, grid, st) : launch_tc<kFmtInt4, false>(tmX, tmW, p, grid, st);
 }
 

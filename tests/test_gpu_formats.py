@@ -45,7 +45,7 @@ GROUPS = [(1056, 32), (1088, 64), (1024, 256), (1024, 1024), (1000, 1000)]
 @pytest.mark.parametrize("M", [1, 5, 16, 40, 200])
 def test_group_sizes_and_symmetric_products(K, g, sym, M):
     N = 520
-    dtype = "bf16" if (M + g) % 2 else "f16"
+    dtype = "bf16" if (M + g + int(sym)) % 2 else "f16"  # both dtypes on every (K, g, M)
     W = gaussian_weights(K, N, 0.02, K + g + M)
     dev_t, (q, sc, z) = _quantize(W, g, sym)
     X = activations(M, K, dtype, M)
@@ -58,11 +58,12 @@ def test_group_sizes_and_symmetric_products(K, g, sym, M):
 @pytest.mark.parametrize("g", [32, 64, 1024])
 @pytest.mark.parametrize("sym", [False, True])
 @pytest.mark.parametrize("M", [16, 32])
-def test_group_sizes_one_hot_rows_are_exact(g, sym, M):
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_group_sizes_one_hot_rows_are_exact(g, sym, M, dtype):
     # one-hot rows reproduce rows of W_hat bit for bit, on both kernels (M = 16:
-    # decode, M = 32: tensor cores), pinning which group each row reads
+    # decode, M = 32: tensor cores), pinning which group each row reads (rows
+    # 31 and 32 straddle a boundary between groups of 32)
     K, N = 1024, 264
-    dtype = "bf16" if sym else "f16"
     W = student_t_weights(K, N, 5, 0.01, g)
     dev_t, (q, sc, z) = _quantize(W, g, sym)
     rng = np.random.default_rng(g + M)
