@@ -182,6 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
   }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  // Programmatic dependent launch: the setup above may overlap the previous
+  // kernel on the stream; nothing the caller owns (X, the weights and their
+  // metadata, Y, the workspace) is touched before that kernel has finished.
+  // The next kernel may then start its own setup on SMs this grid leaves.
+  griddep_wait();
+  griddep_launch_dependents();
   if (FMT == kFmtNF4 && threadIdx.x < 16) bars->cb[threadIdx.x] = p.codebook ? p.codebook[threadIdx.x] : p.cb_builtin.v[threadIdx.x];
   if (FMT == kFmtInt4Act) {
     const int G = p.NG;
@@ -195,10 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       act_tab[i] = v;
     }
-  }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, kTmemCols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -415,6 +421,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
+    // this warp's tokens of D, 8 at a time, with two TMEM loads per wait
+    auto drain_d = [&](auto&& use) {
+      const int c_end = (ep + 1) * part;
+      int c = ep * part;
+      for (; c + 16 <= c_end; c += 16) {
+        uint32_t v[8], u[8];
+        tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
+        tmem_ld_x8(tmem + lane_off + (uint32_t)(c + 8), u);
+        tmem_wait_ld();
+        float f[8], g[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          f[j] = __uint_as_float(v[j]);
+          g[j] = __uint_as_float(u[j]);
+        }
+        use(c, f);
+        use(c + 8, g);
+      }
+      if (c < c_end) {
+        uint32_t v[8];
+        tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
+        tmem_wait_ld();
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+        use(c, f);
+      }
+    };
     bool emitted = false;
     if (done && !*abort && split && p.splits > 1) {
       // Split tile: this CTA's fp32 tile goes to the workspace; the CTA that
@@ -422,13 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (deterministic) and writes Y.
       const size_t tile_floats = (size_t)p.BT * kBN;
       float* mine = p.partial + ((size_t)tt * p.splits + zs) * tile_floats;
-      for (int c = ep * part; c < (ep + 1) * part; c += 8) {
-        uint32_t v[8];
-        tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
-        tmem_wait_ld();
+      drain_d([&](int c, const float (&v)[8]) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mine[(size_t)(c + j) * kBN + nl] = __uint_as_float(v[j]);
-      }
+        for (int j = 0; j < 8; ++j) mine[(size_t)(c + j) * kBN + nl] = v[j];
+      });
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");  // the dequant warps only
       if (dw == 0 && lane == 0) {
         __threadfence();  // release: this CTA's tile is in memory before its ticket moves
@@ -445,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tid = (int)threadIdx.x - 64;  // the dequant warps
         const int nf = p.BT * (kBN / 4);
         const size_t zstride = tile_floats / 4;
+        // every row of Y starts 8-byte aligned (ldy is a multiple of 4)
+        const bool y8 = ((reinterpret_cast<uintptr_t>(p.Y) & 7u) == 0) && (p.ldy & 3) == 0;
         constexpr int kU = 4;
         for (int f0 = tid; f0 < nf; f0 += kU * kDqWarps * 32) {
           float4 acc[kU];
@@ -475,11 +508,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int q = 0; q < 4; ++q) xb[(size_t)t * kBN + l0 + q] = vv[q];
             } else if (m0 + t < p.M) {
+              // lanes l0 .. l0+3 are four consecutive output columns (l0 is a
+              // multiple of 4 within one 64-column half): one 8-byte store
+              // when they are all in range and Y allows it
+              const int oc0 = w0 + (l0 >> 6) * p.hi2 + (l0 & 63);
+              uint16_t* y = p.Y + (size_t)(m0 + t) * p.ldy + oc0;
+              if (oc0 + 3 < p.Nout && y8) {
+                *reinterpret_cast<uint2*>(y) = make_uint2(pack2_rn(vv[0], vv[1], BF16), pack2_rn(vv[2], vv[3], BF16));
+              } else {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int l = l0 + q;
-                const int oc = w0 + (l >> 6) * p.hi2 + (l & 63);
-                if (oc < p.Nout) p.Y[(size_t)(m0 + t) * p.ldy + oc] = (uint16_t)(pack2_rn(vv[q], 0.f, BF16) & 0xFFFFu);
+                for (int q = 0; q < 4; ++q)
+                  if (oc0 + q < p.Nout) y[q] = (uint16_t)(pack2_rn(vv[q], 0.f, BF16) & 0xFFFFu);
               }
             }
           }
@@ -487,15 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       emitted = bars->last != 0;
     } else if (done && !*abort) {
-      for (int c = ep * part; c < (ep + 1) * part; c += 8) {
-        uint32_t v[8];
-        tmem_ld_x8(tmem + lane_off + (uint32_t)c, v);
-        tmem_wait_ld();
-        float f[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
-        emit(c, f);
-      }
+      drain_d(emit);
       emitted = true;
     }
     if (p.silu && emitted) {  // a CTA-uniform condition: every dequant warp gets here or none
@@ -534,8 +565,17 @@ cudaError_t launch_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, const Gemm
   }
   const int smem = smem_fixed<FMT>() + (FMT == kFmtInt4Act ? p.NG * kActTableRowBytes : 0);
   if (smem > kMaxSmem) return cudaErrorInvalidValue;
-  gemm_tc_kernel<FMT, BF16><<<grid, kThreads, smem, st>>>(tmX, tmW, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr_pdl[1];
+  attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr_pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<FMT, BF16>, tmX, tmW, p);
 }
 
 }  // namespace
