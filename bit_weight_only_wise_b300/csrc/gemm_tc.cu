@@ -34,6 +34,8 @@
 // (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "dq_common.cuh"
 #include "sm100.cuh"
 #include "tma_host.h"
@@ -478,51 +480,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t zstride = tile_floats / 4;
         // every row of Y starts 8-byte aligned (ldy is a multiple of 4)
         const bool y8 = ((reinterpret_cast<uintptr_t>(p.Y) & 7u) == 0) && (p.ldy & 3) == 0;
-        constexpr int kU = 4;
-        for (int f0 = tid; f0 < nf; f0 += kU * kDqWarps * 32) {
-          float4 acc[kU];
+        // kU float4s a thread in flight: 8 when every thread has that many
+        // (token tiles of 128 or more), else 4
+        auto sum_splits = [&](auto ku) {
+          constexpr int kU = decltype(ku)::value;
+          for (int f0 = tid; f0 < nf; f0 += kU * kDqWarps * 32) {
+            float4 acc[kU];
 #pragma unroll
-          for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int z = 0; z < p.splits; ++z) {
-            float4 v[kU];
+            for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int z = 0; z < p.splits; ++z) {
+              float4 v[kU];
+#pragma unroll
+              for (int u = 0; u < kU; ++u) {
+                const int f = f0 + u * kDqWarps * 32;
+                v[u] = f < nf ? __ldcg(base + (size_t)z * zstride + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int u = 0; u < kU; ++u) {
+                acc[u].x += v[u].x;
+                acc[u].y += v[u].y;
+                acc[u].z += v[u].z;
+                acc[u].w += v[u].w;
+              }
+            }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
               const int f = f0 + u * kDqWarps * 32;
-              v[u] = f < nf ? __ldcg(base + (size_t)z * zstride + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+              if (f >= nf) continue;
+              const int t = f / (kBN / 4), l0 = 4 * (f % (kBN / 4));
+              const float vv[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+              if (p.silu) {
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-              acc[u].x += v[u].x;
-              acc[u].y += v[u].y;
-              acc[u].z += v[u].z;
-              acc[u].w += v[u].w;
-            }
-          }
+                for (int q = 0; q < 4; ++q) xb[(size_t)t * kBN + l0 + q] = vv[q];
+              } else if (m0 + t < p.M) {
+                // lanes l0 .. l0+3 are four consecutive output columns (l0 is a
+                // multiple of 4 within one 64-column half): one 8-byte store
+                // when they are all in range and Y allows it
+                const int oc0 = w0 + (l0 >> 6) * p.hi2 + (l0 & 63);
+                uint16_t* y = p.Y + (size_t)(m0 + t) * p.ldy + oc0;
+                if (oc0 + 3 < p.Nout && y8) {
+                  *reinterpret_cast<uint2*>(y) = make_uint2(pack2_rn(vv[0], vv[1], BF16), pack2_rn(vv[2], vv[3], BF16));
+                } else {
 #pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int f = f0 + u * kDqWarps * 32;
-            if (f >= nf) continue;
-            const int t = f / (kBN / 4), l0 = 4 * (f % (kBN / 4));
-            const float vv[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
-            if (p.silu) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) xb[(size_t)t * kBN + l0 + q] = vv[q];
-            } else if (m0 + t < p.M) {
-              // lanes l0 .. l0+3 are four consecutive output columns (l0 is a
-              // multiple of 4 within one 64-column half): one 8-byte store
-              // when they are all in range and Y allows it
-              const int oc0 = w0 + (l0 >> 6) * p.hi2 + (l0 & 63);
-              uint16_t* y = p.Y + (size_t)(m0 + t) * p.ldy + oc0;
-              if (oc0 + 3 < p.Nout && y8) {
-                *reinterpret_cast<uint2*>(y) = make_uint2(pack2_rn(vv[0], vv[1], BF16), pack2_rn(vv[2], vv[3], BF16));
-              } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  if (oc0 + q < p.Nout) y[q] = (uint16_t)(pack2_rn(vv[q], 0.f, BF16) & 0xFFFFu);
+                  for (int q = 0; q < 4; ++q)
+                    if (oc0 + q < p.Nout) y[q] = (uint16_t)(pack2_rn(vv[q], 0.f, BF16) & 0xFFFFu);
+                }
               }
             }
           }
-        }
+        };
+        if (nf >= 8 * kDqWarps * 32) sum_splits(std::integral_constant<int, 8>{});
+        else sum_splits(std::integral_constant<int, 4>{});
       }
       emitted = bars->last != 0;
     } else if (done && !*abort) {

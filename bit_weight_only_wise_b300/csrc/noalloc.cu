@@ -10,9 +10,8 @@
 // when the library's code is loaded there.
 //
 // The array's device address is looked up with cudaGetSymbolAddress the first
-// time the entry point runs on a device (with that device current) and cached;
-// that first call therefore must not happen inside a stream capture.  Each
-// call clears the part of the array that must start at zero (the split-K
+// time the entry point runs on a device (with that device current) and cached.
+// Each call clears the part of the array that must start at zero (the split-K
 // tickets) and then runs the ordinary decode kernel with the array as its
 // workspace.  All calls share the one array, so calls that overlap on the GPU
 // (different streams, no ordering between them) race on it and must not be

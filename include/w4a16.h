@@ -252,10 +252,10 @@ w4a16_status nf4_quantize(const float* W, int K, int N, int blocksize, const flo
  * loaded on that GPU until the process exits.  Calls that would need more
  * scratch than that return W4A16_ERR_UNSUPPORTED (with the current split-K
  * plan every M <= 16 fits).  The function allocates and frees nothing.
- *  - The first call on each device looks up the array's address with that
- *    device current and keeps it; make that first call before any stream
- *    capture.  A cudaDeviceReset makes the kept address stale: do not call
- *    this function on a device after resetting it in the same process.
+ *  - The first call on each device looks up the array's address
+ *    (cudaGetSymbolAddress, with that device current) and keeps it.  A
+ *    cudaDeviceReset makes the kept address stale: do not call this function
+ *    on a device after resetting it in the same process.
  *  - Each call clears the scratch area that must start at zero, on `stream`.
  *  - All calls share the one array and it keeps the last call's contents:
  *    calls that may run at the same time on the GPU (different streams with
