@@ -10,11 +10,14 @@
 // (K-major).  The fp32 accumulator D[128 x BT] also lives in TMEM.
 //
 // Pipeline (one CTA, 18 warps):
-//   warp 0     TMA producer: per 64-row K block, the X tile [BT x 64] and the
+//   warp 0     TMA producer: per 64-row K block, lane 0 loads the X tile
+//              [BT x 64] into a ring of 4 shared-memory stages and lane 1 the
 //              packed weight tile [8 word-rows x 128 columns] into a ring of
-//              shared-memory stages (mbarrier with transaction count).
+//              8 (mbarriers with transaction counts).  A weight stage is free
+//              once its dequant group has read it, an X stage once the MMAs
+//              that read it have completed.
 //   warp 1     allocates TMEM; one lane issues the MMAs (4 x K=16 per stage)
-//              and commits them to mbarriers that free the stage and the A
+//              and commits them to mbarriers that free the X stage and the A
 //              buffer.
 //   warps 2-17 dequantize, in four groups of 4 that take the K blocks in
 //              turn (so four blocks' loads, arithmetic and TMEM stores
@@ -50,7 +53,8 @@ namespace {
 constexpr int kBN = 128;       // output columns per CTA (MMA M, TMEM lanes)
 constexpr int kBK = 64;        // K rows per stage
 constexpr int kMaxBT = 256;    // tokens per CTA (MMA N)
-constexpr int kStages = 4;
+constexpr int kXStagesMax = 4;  // X tiles: freed when the MMAs that read them complete
+constexpr int kWStagesMax = 8;  // packed weight tiles: freed when a dequant group has read them
 constexpr int kABufs = 4;
 constexpr int kDqWarps = 16;                      // dequantizing warps
 constexpr int kParts = kDqWarps / 4;              // warps sharing one TMEM lane quarter
@@ -60,7 +64,7 @@ constexpr int kParts = kDqWarps / 4;              // warps sharing one TMEM lane
 constexpr int kDqGroups = 4;
 constexpr int kGroupWarps = kDqWarps / kDqGroups;
 constexpr int kWords = (kBK / 8) / (kGroupWarps / 4);  // packed words per thread per stage
-static_assert(kGroupWarps == 4 && kWords == 8 && kStages % kDqGroups == 0 && kABufs % kDqGroups == 0,
+static_assert(kGroupWarps == 4 && kWords == 8 && kABufs % kDqGroups == 0,
               "each group keeps to its own stages and A buffers; a thread takes a whole stage");
 constexpr int kThreads = 32 * (2 + kDqWarps);
 constexpr int kWStageBytes = (kBK / 8) * kBN * 4;  // 4 KB
@@ -70,8 +74,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 struct __align__(8) Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kXStagesMax];   // X stage landed
+  uint64_t empty[kXStagesMax];  // X stage free
+  uint64_t w_full[kWStagesMax];
+  uint64_t w_empty[kWStagesMax];
   uint64_t a_full[kABufs];
   uint64_t a_empty[kABufs];
   uint64_t d_full;
@@ -91,8 +97,16 @@ template <int FMT>
 constexpr int max_bt() { return FMT == kFmtInt4Act ? 128 : kMaxBT; }
 template <int FMT>
 constexpr int x_stage_bytes() { return max_bt<FMT>() * kBK * 2; }
+// Ring depths (5 or 6 X stages measured 1-6% slower than 4).  Act-order keeps
+// 4 weight stages so that its group table keeps room for 290 groups.
 template <int FMT>
-constexpr int smem_fixed() { return 1024 /* alignment slack */ + kStages * (x_stage_bytes<FMT>() + kWStageBytes) + 1024; }
+constexpr int x_stages() { return FMT == kFmtInt4Act ? 4 : kXStagesMax; }
+template <int FMT>
+constexpr int w_stages() { return FMT == kFmtInt4Act ? 4 : kWStagesMax; }
+template <int FMT>
+constexpr int smem_fixed() {
+  return 1024 /* alignment slack */ + x_stages<FMT>() * x_stage_bytes<FMT>() + w_stages<FMT>() * kWStageBytes + 1024;
+}
 constexpr int kActTableRowBytes = kBN * 4;  // one group: 128 columns x (scale | zero << 16)
 constexpr int kMaxSmem = 227 * 1024;
 
@@ -144,11 +158,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kXStageBytes = x_stage_bytes<FMT>();
+  constexpr int kStages = x_stages<FMT>();
+  constexpr int kWStages = w_stages<FMT>();
+  static_assert(smem_fixed<FMT>() <= kMaxSmem, "the rings fit in shared memory");
   uint8_t* sx = smem;                                                          // kStages X tiles
-  uint32_t* sw = reinterpret_cast<uint32_t*>(smem + kStages * kXStageBytes);  // kStages x 4 KB
-  Bars* bars = reinterpret_cast<Bars*>(smem + kStages * (kXStageBytes + kWStageBytes));
+  uint32_t* sw = reinterpret_cast<uint32_t*>(smem + kStages * kXStageBytes);  // kWStages x 4 KB
+  Bars* bars = reinterpret_cast<Bars*>(smem + kStages * kXStageBytes + kWStages * kWStageBytes);
   // act-order: [G][128] words, (scale bits | zero << 16), after the barriers
-  uint32_t* act_tab = reinterpret_cast<uint32_t*>(smem + kStages * (kXStageBytes + kWStageBytes) + 1024);
+  uint32_t* act_tab = reinterpret_cast<uint32_t*>(smem + kStages * kXStageBytes + kWStages * kWStageBytes + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -172,7 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], kGroupWarps + 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&bars->w_full[s], 1);
+      mbar_init(&bars->w_empty[s], kGroupWarps);
     }
     for (int b = 0; b < kABufs; ++b) {
       mbar_init(&bars->a_full[b], kGroupWarps);
@@ -215,25 +236,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint32_t tx = (uint32_t)(p.BT * kBK * 2 + kWStageBytes);
+    // Lane 0 streams the X tiles, lane 1 the packed weight tiles.  The two
+    // rings are separate so that a weight tile can be loaded as soon as its
+    // dequant group has read the previous one, without waiting for the MMAs
+    // that still read the X tile of the same K block.
+    if (lane < 2) {
+      const bool xl = lane == 0;
+      const int depth = xl ? kStages : kWStages;
+      uint64_t* fullb = xl ? bars->full : bars->w_full;
+      uint64_t* emptyb = xl ? bars->empty : bars->w_empty;
+      const uint32_t tx = xl ? (uint32_t)(p.BT * kBK * 2) : (uint32_t)kWStageBytes;
       int issued = 0;
       for (int it = 0; it < nkb; ++it) {
-        const int s = it % kStages;
-        if (!mbar_wait(&bars->empty[s], ((it / kStages) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) break;
-        mbar_arrive_expect_tx(&bars->full[s], tx);
-        tma_load_2d(sx + s * kXStageBytes, &tmX, &bars->full[s], (kb0 + it) * kBK, m0);
-        // the two 64-column halves of the tile, one box each
-        tma_load_2d(sw + s * (kWStageBytes / 4), &tmW, &bars->full[s], w0, (kb0 + it) * (kBK / 8));
-        tma_load_2d(sw + s * (kWStageBytes / 4) + kWStageBytes / 8, &tmW, &bars->full[s], w0 + p.hiofs,
-                    (kb0 + it) * (kBK / 8));
+        const int s = it % depth;
+        if (!mbar_wait(&emptyb[s], ((it / depth) & 1) ^ 1, abort, p.dev_status, kWaitLimitNs)) break;
+        mbar_arrive_expect_tx(&fullb[s], tx);
+        if (xl) {
+          tma_load_2d(sx + s * kXStageBytes, &tmX, &fullb[s], (kb0 + it) * kBK, m0);
+        } else {
+          // the two 64-column halves of the tile, one box each
+          tma_load_2d(sw + s * (kWStageBytes / 4), &tmW, &fullb[s], w0, (kb0 + it) * (kBK / 8));
+          tma_load_2d(sw + s * (kWStageBytes / 4) + kWStageBytes / 8, &tmW, &fullb[s], w0 + p.hiofs,
+                      (kb0 + it) * (kBK / 8));
+        }
         issued = it + 1;
       }
       if (*abort) {
-        // let every copy this CTA started land before its shared memory goes
+        // let every copy this lane started land before its shared memory goes
         // away: the last phase issued on each stage
-        for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it)
-          (void)mbar_drain(&bars->full[it % kStages], (it / kStages) & 1, kDrainLimitNs);
+        for (int it = (issued > depth ? issued - depth : 0); it < issued; ++it)
+          (void)mbar_drain(&fullb[it % depth], (it / depth) & 1, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -329,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool alive = true;
     for (int it = grp; it < nkb && alive; it += kDqGroups) {
-      const int s = it % kStages;
+      const int s = it % kWStages;
       const int b = it % kABufs;
       if (it > grp) {
         s_raw = s_nxt;
@@ -341,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fetch(kb0 + it + 2 * kStep, s_nx2, z_nx2, am_nx2);
         make_consts();
       }
-      if (!mbar_wait(&bars->full[s], (it / kStages) & 1, abort, p.dev_status, kWaitLimitNs)) {
+      if (!mbar_wait(&bars->w_full[s], (it / kWStages) & 1, abort, p.dev_status, kWaitLimitNs)) {
         alive = false;
         break;
       }
@@ -350,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kWords; ++i) wv[i] = wst[(nl >> 6) * (kBN / 2) * (kBK / 8) + i * (kBN / 2) + (nl & 63)];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->empty[s]);
+      if (lane == 0) mbar_arrive(&bars->w_empty[s]);
       uint32_t regs[4 * kWords];
       if constexpr (FMT == kFmtInt4Act) {
         // every K row has its own group: rows 64*it + 8*i + 2j, +1
