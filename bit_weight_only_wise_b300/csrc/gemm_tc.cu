@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA in flight before TMEM is freed.
     const bool done = mbar_drain(&bars->d_full, 0, kDrainLimitNs);
     tc_fence_after();
+    // One decision for all 16 dequant warps: the branches below hold named
+    // barriers, and each warp reads the abort flag at its own time.
+    const bool stop = bar_red_or(1, kDqWarps * 32, !done || *abort != 0);
     // Fused SiLU: every lane's fp32 results pass through shared memory (the
     // X ring, idle once the MMAs are done: BT x 128 floats), then the gate
     // lanes pair them with the up lanes'.
@@ -484,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     bool emitted = false;
-    if (done && !*abort && split && p.splits > 1) {
+    if (!stop && split && p.splits > 1) {
       // Split tile: this CTA's fp32 tile goes to the workspace; the CTA that
       // completes the tile's ticket sums the splits in split order
       // (deterministic) and writes Y.
@@ -565,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else sum_splits(std::integral_constant<int, 4>{});
       }
       emitted = bars->last != 0;
-    } else if (done && !*abort) {
+    } else if (!stop) {
       drain_d(emit);
       emitted = true;
     }
