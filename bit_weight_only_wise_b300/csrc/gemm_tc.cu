@@ -148,6 +148,19 @@ struct GemmParams {
   uint32_t idesc;
 };
 
+// Named barrier `id` over `nthreads` threads that also ORs a predicate: every
+// participating thread gets the same answer, so a branch on it that leads to
+// further barriers is taken by all of them or by none.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // SiLU(g) * u in fp32, the gate_up epilogue
 __device__ __forceinline__ float silu_mul_f32(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
 

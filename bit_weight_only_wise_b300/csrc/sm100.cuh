@@ -146,19 +146,6 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// Named barrier `id` over `nthreads` threads that also ORs a predicate: every
-// participating thread gets the same answer, so a branch on it that leads to
-// further barriers is taken by all of them or by none.
-__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
 // ------------------------------------------- programmatic dependent launch
 // Wait until the grids this one depends on have completed and their writes are
 // visible (a no-op when launched without a programmatic dependency).
