@@ -314,17 +314,21 @@ def sweep_entry(name, K, N, M, dt, us, nbytes, hbm_peak, tc_peak):
 
 
 def sweep_summary(entries):
-    """The sweep as one flat object of strings, one per timed configuration:
-    "<config> M=<M> KxN dtype" -> "<us> us, <GB/s> GB/s (<hbm frac>), <TFLOP/s>
-    TFLOP/s (<tensor frac>)" -- compact enough to sit in the bench line."""
+    """A short digest of the sweep for the bench line (the full entries are
+    the sweep_entry JSON lines printed before it): how many entries, each
+    configuration's M=1 fraction of the HBM peak, and its largest-M fraction
+    of the tensor peak."""
     if not entries:
         return None
-    out = {}
+    m1, top = {}, {}
     for e in entries:
-        key = f"{e['config']} M={e['M']} {e['K']}x{e['N']} {e['dtype']}"
-        out[key] = (f"{e['us']} us, {e['GBs']} GB/s ({e['hbm_frac']:.3f} hbm), "
-                    f"{e['TFLOPs']} TFLOP/s ({e['tc_frac']:.3f} tc)")
-    return out
+        name = f"{e['config']} {e['K']}x{e['N']} {e['dtype']}"
+        if e["M"] == 1:
+            m1[name] = round(e["hbm_frac"], 3)
+        if name not in top or e["M"] > top[name][0]:
+            top[name] = (e["M"], round(e["tc_frac"], 3))
+    return {"entries": len(entries), "lines": "one sweep_entry JSON line per entry, before this line",
+            "hbm_frac_at_M1": m1, "tc_frac_at_largest_M": {f"{k} M={v[0]}": v[1] for k, v in top.items() if v[0] > 16}}
 
 
 def config_sweep(torch, w4, dev, hbm_peak, tc_peak):
