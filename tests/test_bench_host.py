@@ -101,3 +101,18 @@ def test_sweep_entry_rates():
 def test_stack_xy_bytes():
     assert bench.STACK_XY_BYTES == 64 * 2 * ((5120 + 7168) + (5120 + 5120) + (5120 + 55296) + (27648 + 5120))
     assert bench.STACK_XY_BYTES < bench.STACK_BYTES // 1000  # activations are < 0.1% of the stream at M = 1
+
+
+def test_sweep_digest_is_short_and_keeps_the_fractions():
+    # the bench line carries a digest of the sweep, not the entries (those are
+    # printed one per line before it): the count, each configuration's M = 1
+    # fraction of the HBM peak and its largest-M fraction of the tensor peak
+    entries = [bench.sweep_entry(f"C{c} shape", 4096, 4096 * c, M, "bf16", 10.0 * M ** 0.5, 8 << 20, 8000.0, 2000.0)
+               for c in (1, 2, 3) for M in (1, 16, 256, 4096)]
+    d = bench.sweep_summary(entries)
+    assert d["entries"] == len(entries)
+    assert set(d["hbm_frac_at_M1"]) == {f"C{c} shape 4096x{4096 * c} bf16" for c in (1, 2, 3)}
+    assert d["hbm_frac_at_M1"]["C1 shape 4096x4096 bf16"] == round(entries[0]["hbm_frac"], 3)
+    assert d["tc_frac_at_largest_M"]["C3 shape 4096x12288 bf16 M=4096"] == round(entries[-1]["tc_frac"], 3)
+    assert len(json.dumps(d)) < 1500
+    assert bench.sweep_summary([]) is None
