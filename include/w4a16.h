@@ -65,12 +65,13 @@
  *    0 < K <= W4A16_MAX_K; outside them W4A16_ERR_INVALID_ARG, nothing
  *    launched.
  *  - M == 0 or N == 0 is a valid empty problem: W4A16_OK, nothing launched.
- *  - The decode kernels are launched as programmatic dependents of the
- *    kernel before them on `stream`, so their start overlaps its end.  Until
- *    that kernel has completed they only prefetch weight lines into L2 (the
- *    device's point of coherence, so a prefetch cannot return stale data);
- *    every read of a caller's buffer happens after it.  Callers need no
- *    ordering beyond the stream's.
+ *  - The decode and tensor-core product kernels are launched as programmatic
+ *    dependents of the kernel before them on `stream`, so their start
+ *    overlaps its end.  Until that kernel has completed they only set up
+ *    their own barriers and tensor memory and (decode) prefetch weight lines
+ *    into L2 (the device's point of coherence, so a prefetch cannot return
+ *    stale data); every read or write of a caller's buffer happens after it.
+ *    Callers need no ordering beyond the stream's.
  *  - The dtype of X and Y is `dtype`; scales are always fp16, absmax fp32.
  */
 #ifndef W4A16_H
