@@ -332,13 +332,23 @@ __device__ __forceinline__ void dq_word_nat_bf16(uint32_t w, const DqConstBF16& 
   }
 }
 
+// (ca, cb) * absmax as two IEEE fp32 products (round to nearest, no flush),
+// issued as one packed fp32x2 multiply, then one pair conversion
+__device__ __forceinline__ uint32_t nf4_pair(float ca, float cb, float absmax, bool bf16) {
+  uint64_t x, m, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(ca), "f"(cb));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(m) : "f"(absmax));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(m));
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+  return pack2_rn(lo, hi, bf16);
+}
+
 template <bool BF16>
 __device__ __forceinline__ void dq_word_nat_nf4(uint32_t w, const float* cb, float absmax, uint32_t out[4]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float lo = __fmul_rn(cb[(w >> (8 * j)) & 0xFu], absmax);
-    const float hi = __fmul_rn(cb[(w >> (8 * j + 4)) & 0xFu], absmax);
-    out[j] = pack2_rn(lo, hi, BF16);
+    out[j] = nf4_pair(cb[(w >> (8 * j)) & 0xFu], cb[(w >> (8 * j + 4)) & 0xFu], absmax, BF16);
   }
 }
 
@@ -349,9 +359,7 @@ template <bool BF16>
 __device__ __forceinline__ void dq_word_nf4(uint32_t w, const float* cb, float absmax, uint32_t out[4]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float lo = __fmul_rn(cb[(w >> (4 * j)) & 0xFu], absmax);
-    const float hi = __fmul_rn(cb[(w >> (4 * j + 16)) & 0xFu], absmax);
-    out[j] = pack2_rn(lo, hi, BF16);
+    out[j] = nf4_pair(cb[(w >> (4 * j)) & 0xFu], cb[(w >> (4 * j + 16)) & 0xFu], absmax, BF16);
   }
 }
 
