@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fetch(kb0 + grp, s_raw, z_raw, am);
     fetch(kb0 + grp + kStep, s_nxt, z_nxt, am_nxt);
     fetch(kb0 + grp + 2 * kStep, s_nx2, z_nx2, am_nx2);
-    // constants of rows 0-31 (…0) and 32-63 (…1) of the block
+    // constants of rows 0-31 (names ending in 0) and 32-63 (ending in 1) of the block
     uint32_t zmix0 = 0, s20 = 0, zmix1 = 0, s21 = 0;
     DqConstBF16Fma cbf0{}, cbf1{};
     auto make_consts = [&]() {
