@@ -240,6 +240,41 @@ def test_nf4dq_one_hot_exact(M):
     assert np.array_equal(bits(Y), nf4.nf4_dequant(codes, am_hat, cb, "bf16")[rows])
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_nf4dq_split_tail_all_outputs(dtype):
+    # the tensor-core kernel on 150 column tiles (a full wave of whole tiles
+    # and two tiles split along K) with double-quantized absmax converted per
+    # block by the dequant warps; every output
+    M, K, N = 40, 2048, 150 * 128
+    W = gaussian_weights(K, N, 0.02, 12)
+    cb, codes, _, am_q, s2, am_hat = _nf4dq(W)
+    X = activations(M, K, dtype, 12)
+    Y = w4.nf4dq_gemm(X.cuda(), to_dev_u32(int4.pack_along_k(codes)), to_dev(am_q), to_dev(s2), to_dev(cb))
+    torch.cuda.synchronize()
+    w_hat = numerics.dtype_bits_to_f64(nf4.nf4_dequant(codes, am_hat, cb, dtype), dtype)
+    Y_ref, A = product.reference(X.double().numpy(), w_hat)
+    assert_close(to_f64(Y), Y_ref, A, f"nf4dq split tail {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("sym", [False, True])
+def test_groups_of_32_split_tail_all_outputs(dtype, sym):
+    # groups of 32 rows (the tensor-core kernel's two-halves format, each
+    # 64-row block carrying two groups) on 150 column tiles, two of them split
+    # along K into ranges that start mid-way through the groups' K; every
+    # output, and bit-equal across two runs
+    M, K, N = 17, 1056, 150 * 128
+    W = gaussian_weights(K, N, 0.02, 32 + int(sym))
+    dev_t, (q, sc, z) = _quantize(W, 32, sym)
+    X = activations(M, K, dtype, 33)
+    Y1 = w4.gemm(X.cuda(), *dev_t[:3], group_size=32)
+    Y2 = w4.gemm(X.cuda(), *dev_t[:3], group_size=32)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    Y_ref, A = _expected(q, sc, z, 32, dtype, X)
+    assert_close(to_f64(Y1), Y_ref, A, f"g=32 split tail sym={sym} {dtype}")
+
+
 # ---------------------------------------------------------------- AWQ layout
 @pytest.mark.parametrize("sym", [False, True])
 @pytest.mark.parametrize("K,N,g", [(1024, 520, 128), (2048, 4104, 64)])
